@@ -1,0 +1,537 @@
+"""Benchmark of the GDN hot path on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+                    [--workload decode|verify|prefill_kda|prefill_varlen]
+
+Default workload (the headline): batched decode, 64 sequences x 1 token,
+H=16, D_k=D_v=128, GDA gate, bf16 q/k/v, fp32 state ~N(0, 0.05); one step is
+one decode step (64 tokens) through gdn_forward. Prints ONE JSON line on rank
+0. Inputs are resident in HBM when the timed region starts; the state chain
+rotates over enough banks that the working set is several times the L2, so
+every step reads its state from HBM. The "e2e" figure repeats the measurement
+with each step's tokens copied from pinned host memory and the outputs copied
+back, inside the timed region.
+
+--impl reference times the fp64 CPU oracle (a deliberately slow baseline) on
+the same workload, on this host's cores, on a bounded sample per step.
+Under torchrun every rank runs its own replica (weak scaling); the time is the
+max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_net_02_gb300 import inputs  # noqa: E402
+
+METRIC = "GDN tokens/s (decode, verify, prefill); % of HBM GB/s or tensor peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------- utilities
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_delta_net_02_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, sha):
+    """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary,
+    if it was taken on the current kernel source (same hash)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.strip().strip("|").split("|")
+                parts = [p.strip() for p in parts]
+                if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == sha:
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        return rows
+
+
+def summarize_clocks(rows, t0, t1):
+    """Median SM clock and active throttle reasons of the samples taken while
+    the timed region ran (wall-clock window [t0, t1])."""
+    import datetime
+    picked = []
+    for r in rows:
+        if len(r) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            continue
+        picked.append((ts, r))
+    inside = [r for ts, r in picked if t0 <= ts <= t1]
+    note = "samples inside the timed region"
+    if not inside and picked:
+        # region shorter than the sampling period: nearest samples around it
+        near = sorted(picked, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:3]
+        inside = [r for _, r in near]
+        note = "timed region shorter than the sampling period; nearest samples"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"],
+                "samples": 0}
+    sm = [float(r[2]) for r in inside if r[2].strip().replace(".", "").isdigit()]
+    smax = [float(r[3]) for r in inside if r[3].strip().replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in inside for i in range(4)
+                      if r[6 + i].strip().lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def timed_graph_steps(graphs, K, stream):
+    """Replays `graphs` (list of (graph, n_steps)) to cover exactly K steps;
+    returns elapsed ms from CUDA events on `stream`."""
+    plan = []
+    left = K
+    full, full_n = graphs[0]
+    while left >= full_n:
+        plan.append(full)
+        left -= full_n
+    for g, n in graphs[1:]:
+        if left >= n:
+            plan.append(g)
+            left -= n
+    assert left == 0, "graph plan does not cover K"
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for g in plan:
+        g.replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def capture(fn_steps, stream, steps):
+    """CUDA graph of `steps` consecutive calls fn_steps(i) for i in steps."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in steps:
+            fn_steps(i)
+    return g
+
+
+# ----------------------------------------------------------------- workloads
+
+class Decode:
+    """64 sequences x 1 token, H=16, D=128, GDA, bf16 q/k/v, fp32 state."""
+    N, H, D = 64, 16, 128
+    POOL = 256      # distinct token steps resident on the device
+    BANKS = 8       # rotating state banks (8 x 64 MiB = 512 MiB > 3 x L2)
+    name = "decode"
+
+    @property
+    def tokens_per_step(self):
+        return self.N
+
+    def config(self):
+        return {"workload": "batched decode: 64 sequences x 1 token, H=16, D_k=D_v=128, GDA "
+                            "scalar gate, bf16 q/k/v, fp32 state ~N(0,0.05), K=1 slot",
+                "n_seqs": self.N, "heads": self.H, "D_k": self.D, "D_v": self.D,
+                "tokens_per_step": self.N, "input_dtype": "bf16", "state_dtype": "f32",
+                "l2": f"inputs larger than L2: the state chain rotates over {self.BANKS} "
+                      f"banks of 64 MiB and {self.POOL} distinct token steps",
+                "timing": "CUDA graphs of consecutive steps, CUDA events on the launch stream"}
+
+    def alg_bytes_per_step(self):
+        D = self.D
+        per = 8 * D * D + (2 * D + D) * 2 + 4 + 4 + 4 * D   # 132,360 B per token-head
+        return per * self.N * self.H
+
+    def setup(self, gdn, dev):
+        N, H, D = self.N, self.H, self.D
+        self.gdn = gdn
+        self.banks = [inputs.decode_state(1, N, H, D).to(dev) for _ in range(1)]
+        for _ in range(self.BANKS - 1):
+            self.banks.append(torch.empty_like(self.banks[0]))
+        self.bank_ptrs = [gdn.state_ptr_array(gdn.per_seq_state_ptrs(b, N), dev)
+                          for b in self.banks]
+        toks = [inputs.decode_tokens(1, s, N, H, D) for s in range(self.POOL)]
+        self.host = [torch.stack([t[i] for t in toks]) for i in range(5)]  # q,k,v,g,beta
+        self.dev = [h.to(dev) for h in self.host]
+        self.out = torch.empty(N, H, D, device=dev)
+        self.shape = gdn.gdn_shape(N, 1, H, D, D, gdn.GDN_BF16, D ** -0.5)
+        # e2e: pinned host pool, device staging, pinned host output
+        self.pinned = [h.pin_memory() for h in self.host]
+        self.stage = [torch.empty_like(d[0]) for d in self.dev]
+        self.out_host = torch.empty(N, H, D, dtype=torch.float32).pin_memory()
+        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.d2h_bytes = self.out.numel() * 4
+
+    def step(self, i, stream):
+        p = i % self.POOL
+        src = i % self.BANKS
+        dst = (i + 1) % self.BANKS
+        q, k, v, g, beta = (t[p] for t in self.dev)
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[src],
+                             self.banks[dst], self.out, 1, "gda", stream)
+
+    def step_e2e(self, i, stream):
+        p = i % self.POOL
+        for s, h in zip(self.stage, self.pinned):
+            s.copy_(h[p], non_blocking=True)
+        src = i % self.BANKS
+        dst = (i + 1) % self.BANKS
+        q, k, v, g, beta = self.stage
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[src],
+                             self.banks[dst], self.out, 1, "gda", stream)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def graph_len(self):
+        return self.POOL  # a multiple of BANKS: replays continue the chain
+
+    # ---- CPU oracle on a bounded sample of the same workload
+    def oracle_step_fn(self, n_seqs):
+        import oracle
+        N, H, D = self.N, self.H, self.D
+        st = inputs.to_f64(inputs.decode_state(1, N, H, D)[:n_seqs])
+        pool = [inputs.decode_tokens(1, s, N, H, D) for s in range(4)]
+        pool = [[inputs.to_f64(t[:n_seqs]) for t in toks] for toks in pool]
+        state = {"S": st, "i": 0}
+
+        def run():
+            q, k, v, g, beta = pool[state["i"] % len(pool)]
+            _, S, _ = oracle.forward(q, k, v, g, beta, state["S"], scale=D ** -0.5)
+            state["S"] = S
+            state["i"] += 1
+            return n_seqs  # tokens processed
+        return run
+
+
+class Verify(Decode):
+    """32 sequences x T=8 tokens (draft_max 7), K=8 slots, H=16, D=128, GDA."""
+    N, T, K, H, D = 32, 8, 8, 16, 128
+    POOL = 64
+    BANKS = 4
+    name = "verify"
+
+    @property
+    def tokens_per_step(self):
+        return self.N * self.T
+
+    def config(self):
+        return {"workload": "speculative verify: 32 sequences x T=8 tokens, K=8 snapshot slots, "
+                            "H=16, D_k=D_v=128, GDA, bf16 q/k/v, fp32 state",
+                "n_seqs": self.N, "T": self.T, "n_slots": self.K, "heads": self.H,
+                "tokens_per_step": self.N * self.T, "input_dtype": "bf16",
+                "l2": "inputs larger than L2: 256 MiB of slots written per call, "
+                      f"{self.BANKS} rotating input-state banks",
+                "timing": "CUDA graphs of consecutive calls, CUDA events on the launch stream"}
+
+    def alg_bytes_per_step(self):
+        D = self.D
+        per_seq_head = 4 * D * D * (1 + self.K) + self.T * ((2 * D + D) * 2 + 8 + 4 * D)
+        return per_seq_head * self.N * self.H
+
+    def setup(self, gdn, dev):
+        N, T, H, D, K = self.N, self.T, self.H, self.D, self.K
+        self.gdn = gdn
+        base = inputs.verify_batch(2, N, T, H, D, K)
+        self.banks = [base.state.to(dev)] + [
+            (base.state + 0.001 * j).to(dev) for j in range(1, self.BANKS)]
+        self.bank_ptrs = [gdn.state_ptr_array(gdn.per_seq_state_ptrs(b, N), dev)
+                          for b in self.banks]
+        pool = [inputs.make_batch(1000 + s, [T] * N, H, D, D, n_slots=K, state_std=0.0)
+                for s in range(self.POOL)]
+        self.host = [torch.stack([getattr(b, n) for b in pool])
+                     for n in ("q", "k", "v", "g", "beta")]
+        self.dev = [h.to(dev) for h in self.host]
+        self.slots = torch.empty(N, K, H, D, D, device=dev)
+        self.out = torch.empty(N * T, H, D, device=dev)
+        self.shape = gdn.gdn_shape(N, T, H, D, D, gdn.GDN_BF16, D ** -0.5)
+        self.pinned = [h.pin_memory() for h in self.host]
+        self.stage = [torch.empty_like(d[0]) for d in self.dev]
+        self.out_host = torch.empty(N * T, H, D, dtype=torch.float32).pin_memory()
+        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.d2h_bytes = self.out.numel() * 4
+
+    def step(self, i, stream):
+        p = i % self.POOL
+        q, k, v, g, beta = (t[p] for t in self.dev)
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
+                             self.slots, self.out, self.K, "gda", stream)
+
+    def step_e2e(self, i, stream):
+        p = i % self.POOL
+        for s, h in zip(self.stage, self.pinned):
+            s.copy_(h[p], non_blocking=True)
+        q, k, v, g, beta = self.stage
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
+                             self.slots, self.out, self.K, "gda", stream)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def graph_len(self):
+        return self.POOL
+
+    def oracle_step_fn(self, n_seqs):
+        import oracle
+        b = inputs.verify_batch(2, self.N, self.T, self.H, self.D, self.K)
+        sl = slice(0, n_seqs * self.T)
+        args = [inputs.to_f64(getattr(b, n)[sl]) for n in ("q", "k", "v", "g", "beta")]
+        S0 = inputs.to_f64(b.state[:n_seqs])
+
+        def run():
+            oracle.forward(*args, S0, scale=self.D ** -0.5, n_slots=self.K)
+            return n_seqs * self.T
+        return run
+
+
+WORKLOADS = {"decode": Decode, "verify": Verify}
+
+
+# ----------------------------------------------------------------- arms
+
+def run_cpu_baseline(wl, budget_s=15.0):
+    """The oracle, as it stands, on this host's cores, on a bounded sample."""
+    import oracle
+    cores = oracle.max_threads()
+    n_seqs = wl.N
+    fn = wl.oracle_step_fn(n_seqs)
+    t = time.perf_counter()
+    fn()
+    one = time.perf_counter() - t
+    reps = max(1, min(200, int(budget_s / max(one, 1e-6))))
+    tok = 0
+    t = time.perf_counter()
+    for _ in range(reps):
+        tok += fn()
+    el = time.perf_counter() - t
+    return {"value": tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full steps of the same workload ({n_seqs} sequences each), "
+                      f"fp64, {el:.1f} s"}
+
+
+def reference_arm(args, wl_cls):
+    ws, rank, local = dist_env()
+    wl = wl_cls()
+    if rank != 0:
+        return 0
+    import oracle
+    cores = oracle.max_threads()
+    # size each step's sample so that warmup + steps take about a minute
+    probe = wl.oracle_step_fn(1)
+    t = time.perf_counter()
+    probe()
+    per_seq = time.perf_counter() - t
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n_seqs = int(max(1, min(wl.N, budget / max(per_seq, 1e-6))))
+    fn = wl.oracle_step_fn(n_seqs)
+    for _ in range(args.warmup):
+        fn()
+    tok = 0
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        tok += fn()
+    el = time.perf_counter() - t
+    val = tok / el
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": wl.config(),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {n_seqs} of {wl.N} sequences of the "
+                                       f"workload, fp64 oracle on host cores"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gdn_arm(args, wl_cls):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from gated_delta_net_02_gb300 import build
+    build.build()
+    from gated_delta_net_02_gb300 import gdn
+
+    wl = wl_cls()
+    wl.setup(gdn, dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    L = wl.graph_len()
+    K, W = args.steps, args.warmup
+
+    def graphs_for(step_fn):
+        gs = []
+        with torch.cuda.stream(stream):
+            gs.append((capture(lambda i: step_fn(i, stream), stream, range(L)), L))
+            rem = K % L
+            if rem:
+                gs.append((capture(lambda i: step_fn(i, stream), stream, range(rem)), rem))
+        return gs
+
+    # warm-up: W eager steps (also initialises per-device state before capture)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            wl.step(i, stream)
+    stream.synchronize()
+    gdn.gdn_check_device_error(stream)
+    graphs = graphs_for(wl.step)
+    for g, _ in graphs:  # one untimed replay uploads each graph
+        g.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3)
+    barrier()
+    t_wall0 = time.time()
+    ms = timed_graph_steps(graphs, K, stream)
+    t_wall1 = time.time()
+    barrier()
+    time.sleep(0.15)
+    clock_rows = sampler.stop() if sampler else []
+    gdn.gdn_check_device_error(stream)
+
+    # e2e: host tokens in, host outputs back, per step, same K
+    graphs_e2e = graphs_for(wl.step_e2e)
+    for g, _ in graphs_e2e:
+        g.replay()
+    stream.synchronize()
+    barrier()
+    ms_e2e = timed_graph_steps(graphs_e2e, K, stream)
+    barrier()
+    gdn.gdn_check_device_error(stream)
+
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max, ms_e2e_max = t.tolist()
+    tokens_all = wl.tokens_per_step * K * ws
+    value = tokens_all / (ms_max / 1e3)
+    e2e_value = tokens_all / (ms_e2e_max / 1e3)
+
+    if rank == 0:
+        peaks, src = measured_peaks()
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        kern_s = ms / K / 1e3  # this rank's average launch duration
+        achieved = wl.alg_bytes_per_step() / kern_s / 1e9
+        sha = source_sha("recurrent.cu", "common.cuh")
+        traffic = ncu_traffic("gdn_recurrent_" + wl.name, sha)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": K, "warmup": W, "ms_per_step": ms_max / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": wl.config(),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic,
+                         "kernel": "recurrent_kernel (gdn_forward)",
+                         "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
+                         "peak_source": f"{src} hbm_gbs"},
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
+            "gpu_launches": K,
+            "clocks": summarize_clocks(clock_rows, t_wall0, t_wall1),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20480)
+    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl_cls = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, wl_cls)
+    return gdn_arm(args, wl_cls)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

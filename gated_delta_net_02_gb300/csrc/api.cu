@@ -1,0 +1,324 @@
+// api.cu -- the C ABI of libgdn (declared in include/gdn.h): argument
+// validation, dispatch to the kernels, error reporting, the per-device error
+// word and the host-side rollback table.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "gdn.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_msg;
+
+gdn_status fail(gdn_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return st;
+}
+
+gdn_status ok() { return GDN_OK; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_size_ok(int d) { return d == 64 || d == 128; }
+
+}  // namespace
+
+// One error word per device; kernels receive its device address.
+__device__ int g_gdn_err_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+int *g_err_ptr[kMaxDevices] = {};
+
+// Device address of the current device's error word, looked up once per
+// device with that device current.
+gdn_status device_err_ptr(int **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gdn_err_word);
+    if (e != cudaSuccess)
+      return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(error word): %s",
+                  cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<int *>(p);
+  }
+  *out = g_err_ptr[dev];
+  return GDN_OK;
+}
+
+gdn_status check_launch(cudaError_t e, const char *what) {
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_last_error(void) { return g_msg.c_str(); }
+
+const char *gdn_version(void) { return "libgdn 0.1.0 (sm_103a)"; }
+
+gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
+                       const void *v, const float *g, const float *beta,
+                       const float *const *state_in, float *state_slots,
+                       float *out, int n_slots, gdn_mode mode,
+                       gdn_stream_t stream) {
+  if (!shape) return fail(GDN_ERR_INVALID_ARG, "gdn_forward: shape is NULL");
+  const gdn_shape &s = *shape;
+  if (s.n_seqs < 0 || s.T < 0 || s.H <= 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: n_seqs=%d T=%d H=%d", s.n_seqs, s.T, s.H);
+  if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: mode %d", (int)mode);
+  if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: in_dtype %d", (int)s.in_dtype);
+  if (n_slots < 1)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: n_slots=%d (need >= 1)", n_slots);
+  if (s.D_k <= 0 || s.D_v <= 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: D_k=%d D_v=%d", s.D_k, s.D_v);
+  if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward: head sizes D_k=%d D_v=%d (supported: 64, 128)",
+                s.D_k, s.D_v);
+  if (!std::isfinite(s.scale))
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: scale is not finite");
+  const long long ntok = (long long)s.n_seqs * s.T;
+  if (ntok > (1LL << 31) / s.H)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward: %lld tokens x %d heads too large", ntok, s.H);
+  if (s.n_seqs == 0) return ok();
+  if (!state_in || !state_slots)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: state_in/state_slots is NULL");
+  if (!aligned16(state_in) || !aligned16(state_slots))
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: state buffers must be 16-byte aligned");
+  if (ntok == 0) return ok();
+  const void *ptrs[] = {q, k, v, g, beta, out};
+  const char *names[] = {"q", "k", "v", "g", "beta", "out"};
+  for (int i = 0; i < 6; ++i) {
+    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward: %s is NULL", names[i]);
+    if (!aligned16(ptrs[i]))
+      return fail(GDN_ERR_INVALID_ARG, "gdn_forward: %s is not 16-byte aligned", names[i]);
+  }
+  int *err = nullptr;
+  gdn_status st = device_err_ptr(&err);
+  if (st != GDN_OK) return st;
+
+  gdn::RecurrentArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state_in = state_in; a.slots = state_slots; a.out = out;
+  a.tok_start = nullptr; a.seq_len = nullptr;
+  a.n_seqs = s.n_seqs; a.T = s.T; a.H = s.H; a.Dk = s.D_k; a.Dv = s.D_v;
+  a.n_slots = n_slots;
+  a.kda = mode == GDN_MODE_KDA;
+  a.bf16 = s.in_dtype == GDN_BF16;
+  a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
+  a.err = err;
+  return check_launch(gdn::launch_recurrent(a, reinterpret_cast<cudaStream_t>(stream)),
+                      "gdn_forward launch");
+}
+
+size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots) {
+  if (!shape || shape->n_seqs <= 0 || shape->total_tokens < 0 || shape->H <= 0 ||
+      n_slots < 1)
+    return 0;
+  return gdn::chunked_workspace_size(shape->n_seqs, shape->total_tokens, shape->H,
+                                     shape->D_k, shape->D_v, n_slots);
+}
+
+gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
+                               const int32_t *cu_seqlens, const void *q,
+                               const void *k, const void *v, const float *g,
+                               const float *beta, const float *const *state_in,
+                               float *state_slots, float *out, int n_slots,
+                               gdn_mode mode, void *workspace,
+                               size_t workspace_bytes, gdn_stream_t stream) {
+  if (!shape) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: shape is NULL");
+  const gdn_varlen_shape &s = *shape;
+  if (s.n_seqs <= 0 || s.total_tokens < 0 || s.H <= 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: n_seqs=%d total_tokens=%d H=%d",
+                s.n_seqs, s.total_tokens, s.H);
+  if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: mode %d", (int)mode);
+  if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: in_dtype %d", (int)s.in_dtype);
+  if (n_slots < 1)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: n_slots=%d (need >= 1)", n_slots);
+  if (s.D_k != 128 || s.D_v != 128)
+    return fail(GDN_ERR_UNSUPPORTED,
+                "gdn_forward_chunked: tensor-core path needs D_k = D_v = 128 (got %d, %d)",
+                s.D_k, s.D_v);
+  if (s.in_dtype != GDN_BF16)
+    return fail(GDN_ERR_UNSUPPORTED,
+                "gdn_forward_chunked: bf16 inputs only (fp32 inputs: use gdn_forward)");
+  if (!std::isfinite(s.scale))
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: scale is not finite");
+  if ((long long)s.total_tokens * s.H > (1LL << 31))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward_chunked: too many token-heads");
+  const void *ptrs[] = {cu_seqlens, state_in, state_slots, workspace};
+  const char *names[] = {"cu_seqlens", "state_in", "state_slots", "workspace"};
+  for (int i = 0; i < 4; ++i)
+    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is NULL", names[i]);
+  if (s.total_tokens > 0) {
+    const void *tp[] = {q, k, v, g, beta, out};
+    const char *tn[] = {"q", "k", "v", "g", "beta", "out"};
+    for (int i = 0; i < 6; ++i) {
+      if (!tp[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is NULL", tn[i]);
+      if (!aligned16(tp[i]))
+        return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is not 16-byte aligned", tn[i]);
+    }
+  }
+  if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: buffers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: workspace must be 256-byte aligned");
+  const size_t need = gdn_chunked_workspace_size(shape, n_slots);
+  if (workspace_bytes < need)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  int *err = nullptr;
+  gdn_status st = device_err_ptr(&err);
+  if (st != GDN_OK) return st;
+
+  gdn::ChunkedArgs a{};
+  a.cu_seqlens = cu_seqlens;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state_in = state_in; a.slots = state_slots; a.out = out;
+  a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
+  a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
+  a.kda = mode == GDN_MODE_KDA;
+  a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.err = err;
+  return check_launch(gdn::launch_chunked(a, reinterpret_cast<cudaStream_t>(stream)),
+                      "gdn_forward_chunked launch");
+}
+
+// ---- rollback table --------------------------------------------------------
+
+struct gdn_seq_table {
+  int n_seqs;
+  int n_slots;
+  std::vector<int> T_last;  // tokens of each sequence's last forward
+};
+
+gdn_status gdn_seq_table_create(int n_seqs, int n_slots, gdn_seq_table **out) {
+  if (!out) return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_create: out is NULL");
+  *out = nullptr;
+  if (n_seqs < 0 || n_slots < 1)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_create: n_seqs=%d n_slots=%d", n_seqs, n_slots);
+  gdn_seq_table *t = new (std::nothrow) gdn_seq_table;
+  if (!t) return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_create: out of host memory");
+  t->n_seqs = n_seqs;
+  t->n_slots = n_slots;
+  t->T_last.assign((size_t)n_seqs, 0);
+  *out = t;
+  return GDN_OK;
+}
+
+void gdn_seq_table_destroy(gdn_seq_table *table) { delete table; }
+
+gdn_status gdn_seq_table_record(gdn_seq_table *t, int seq, int T_last) {
+  if (!t) return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_record: table is NULL");
+  if (seq < 0 || seq >= t->n_seqs || T_last < 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_record: seq=%d T_last=%d", seq, T_last);
+  t->T_last[(size_t)seq] = T_last;
+  return GDN_OK;
+}
+
+gdn_status gdn_seq_table_clear(gdn_seq_table *t, int seq) {
+  if (!t) return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_clear: table is NULL");
+  if (seq < 0 || seq >= t->n_seqs)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_seq_table_clear: seq=%d", seq);
+  t->T_last[(size_t)seq] = 0;
+  return GDN_OK;
+}
+
+gdn_status gdn_rollback(const gdn_seq_table *t, int seq, int n_accepted, int *slot) {
+  if (!t || !slot) return fail(GDN_ERR_INVALID_ARG, "gdn_rollback: NULL argument");
+  if (seq < 0 || seq >= t->n_seqs)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_rollback: seq=%d of %d", seq, t->n_seqs);
+  const int T = t->T_last[(size_t)seq];
+  const int K = t->n_slots;
+  if (n_accepted < 0 || n_accepted > T)
+    return fail(GDN_ERR_ROLLBACK_RANGE, "gdn_rollback: n_accepted=%d outside [0, %d]",
+                n_accepted, T);
+  if (n_accepted == 0) {
+    *slot = -1;
+    return GDN_OK;
+  }
+  // The state after token n_accepted-1 was stored iff that token is one of
+  // the last K tokens of the forward.
+  const int j = (n_accepted - 1) - (T - K);
+  if (j < 0)
+    return fail(GDN_ERR_ROLLBACK_RANGE,
+                "gdn_rollback: state after %d of %d tokens was not stored (K=%d)",
+                n_accepted, T, K);
+  *slot = j;
+  return GDN_OK;
+}
+
+gdn_status gdn_slot_state_ptr(const float *state_slots, int seq, int slot,
+                              int n_slots, int H, int D_k, int D_v,
+                              const float **out) {
+  if (!out) return fail(GDN_ERR_INVALID_ARG, "gdn_slot_state_ptr: out is NULL");
+  if (slot == -1) {
+    *out = nullptr;
+    return GDN_OK;
+  }
+  if (!state_slots || seq < 0 || slot < 0 || slot >= n_slots || H <= 0 || D_k <= 0 || D_v <= 0)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_slot_state_ptr: seq=%d slot=%d n_slots=%d", seq,
+                slot, n_slots);
+  const long long per = (long long)H * D_k * D_v;
+  *out = state_slots + ((long long)seq * n_slots + slot) * per;
+  return GDN_OK;
+}
+
+gdn_status gdn_check_device_error(gdn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn_check_device_error: %s", cudaGetErrorString(e));
+  int *dummy = nullptr;
+  gdn_status st = device_err_ptr(&dummy);
+  if (st != GDN_OK) return st;
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_gdn_err_word, sizeof(int));
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn_check_device_error: %s", cudaGetErrorString(e));
+  if (word == 0) return GDN_OK;
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_gdn_err_word, &zero, sizeof(int));
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn_check_device_error: %s", cudaGetErrorString(e));
+  switch (word) {
+    case gdn::kDevTimeout:
+      return fail(GDN_ERR_TIMEOUT, "a device-side wait ran out (kernel abandoned its work)");
+    case gdn::kDevBadSeqlens:
+      return fail(GDN_ERR_DEVICE_ARG, "cu_seqlens is not a valid offset table");
+    case gdn::kDevOverlap:
+      return fail(GDN_ERR_DEVICE_ARG, "a state_in pointer points into state_slots");
+    default:
+      return fail(GDN_ERR_DEVICE_ARG, "device error word %d", word);
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels. Host-only declarations; no CUDA types beyond cudaStream_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Recurrent (token-loop) forward over n_seqs sequences of one head group.
+struct RecurrentArgs {
+  const void *q, *k, *v;        // [Ntok][H][Dk|Dv], bf16 or fp32
+  const float *g, *beta;        // [Ntok][H](x Dk for KDA), [Ntok][H]
+  const float *const *state_in; // device [n_seqs] pointers, NULL = zero
+  float *slots;                 // [n_seqs][n_slots][H][Dk][Dv]
+  float *out;                   // [Ntok][H][Dv]
+  const int *tok_start;         // device [n_seqs] first token, or NULL (s*T)
+  const int *seq_len;           // device [n_seqs] tokens, or NULL (T)
+  int n_seqs, T, H, Dk, Dv, n_slots;
+  bool kda, bf16;
+  float scale;
+  int *err;                     // device error word
+};
+
+cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);
+
+// Chunked (tensor-core) prefill of varlen sequences; see chunked.cu.
+struct ChunkedArgs {
+  const int32_t *cu_seqlens;    // device [n_seqs + 1]
+  const void *q, *k, *v;        // bf16
+  const float *g, *beta;
+  const float *const *state_in; // device [n_seqs]
+  float *slots;
+  float *out;
+  int n_seqs, total_tokens, H, Dk, Dv, n_slots;
+  bool kda;
+  float scale;
+  void *workspace;
+  size_t workspace_bytes;
+  int *err;
+};
+
+size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk,
+                              int Dv, int n_slots);
+cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,198 @@
+/*
+ * gdn.h -- C ABI of libgdn, the gated delta-net (GDN) recurrence on NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The op. Per sequence s, head h and token t, the D_k x D_v fp32 state S of
+ * that head (row i = key index, column j = value index) is
+ *   decayed    S <- exp(g) S               (GDA: one gate per head and token)
+ *              S[i,:] <- exp(g_i) S[i,:]   (KDA: one gate per key row)
+ *   read       u = S^T k
+ *   corrected  d = beta (v - u)
+ *   written    S <- S + k d^T
+ *   queried    o = scale S^T q             (after the write)
+ * This is the gated delta rule of "Gated Delta Networks" (Yang, Kautz,
+ * Hatamizadeh, ICLR 2025); the op is GGML_OP_GATED_DELTA_NET with the GDA and
+ * KDA modes and head sizes 64/128 of "metal : add GDN kernel (#20361)"
+ * (llama.cpp commits, tag b9752, src/models/qwen35.cpp). g is a log-decay used
+ * as exp(g) with no clamp; beta is used as given (the caller applies any
+ * sigmoid); q and k are used as given (the caller normalises them).
+ *
+ * Snapshots and rollback ("metal: add GDN partial rollback" and "llama: allow
+ * partial seq_rm for GDN models for speculative decoding", koboldcpp commits,
+ * tag v1.113.1): a forward keeps K = n_slots states per sequence. After token
+ * t of a T-token sequence with t >= T-K the state goes to slot t-(T-K), so
+ * slot K-1 is the final state and K = 1 is the plain single-state forward.
+ * When T < K, slots j < K-T are not written. The input state is a separate
+ * buffer and is never written. Rolling back to n accepted tokens is a slot
+ * select (gdn_rollback), not a recompute.
+ *
+ * Conventions for every call below.
+ *  - Ownership: the caller allocates and owns every buffer and the stream.
+ *    The library allocates no device memory on these calls and never
+ *    synchronises the stream, except gdn_check_device_error.
+ *  - Layouts: dense, row-major, innermost index last, exactly as written in
+ *    each comment; no strides. Ntok is the number of packed tokens.
+ *  - Alignment: every device buffer must be 16-byte aligned.
+ *  - Supported shapes: D_k, D_v in {64, 128}. Anything else returns
+ *    GDN_ERR_UNSUPPORTED; there is no fallback path of any kind.
+ *  - Errors: every call returns a gdn_status; gdn_last_error() gives the
+ *    calling thread's last message. Kernel launches are asynchronous: a
+ *    condition only the device can see (a bad cu_seqlens entry, a bounded
+ *    wait that ran out) sets a per-device error word that
+ *    gdn_check_device_error reads and clears.
+ *  - Streams: gdn_stream_t is a cudaStream_t (NULL = the legacy default).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gdn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned buffer, overlap */
+  GDN_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. D_k = 32) */
+  GDN_ERR_ROLLBACK_RANGE = 3, /* the requested state was not stored */
+  GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  GDN_ERR_TIMEOUT = 5,        /* a bounded device-side wait ran out */
+  GDN_ERR_DEVICE_ARG = 6      /* the device found a bad argument (cu_seqlens) */
+} gdn_status;
+
+typedef enum { GDN_MODE_GDA = 0, GDN_MODE_KDA = 1 } gdn_mode;
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char *gdn_last_error(void);
+
+/* Version string of the library. */
+const char *gdn_version(void);
+
+/* ------------------------------------------------------------------------
+ * Uniform-length forward: decode (T = 1) and speculative verify
+ * (T = draft_max + 1). Runs the token recurrence on the recurrent kernel.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int n_seqs;         /* N >= 0 independent sequences */
+  int T;              /* tokens per sequence, >= 0 */
+  int H;              /* heads (q, k, v all have H heads) */
+  int D_k, D_v;       /* head sizes, each 64 or 128 */
+  gdn_dtype in_dtype; /* dtype of q, k, v; g and beta are always fp32 */
+  float scale;        /* output scale; 0 means 1/sqrt(D_k) */
+} gdn_shape;
+
+/*
+ * q, k        device [N*T][H][D_k]  in_dtype   (token n*T+t is token t of seq n)
+ * v           device [N*T][H][D_v]  in_dtype
+ * g           device fp32 [N*T][H] (GDA) or [N*T][H][D_k] (KDA)
+ * beta        device fp32 [N*T][H]
+ * state_in    device array of N device pointers; state_in[s] -> fp32
+ *             [H][D_k][D_v], the state before this call (any slot a rollback
+ *             chose). A NULL entry means a zero state. Read only.
+ * state_slots device fp32 [N][n_slots][H][D_k][D_v]; slot j of sequence s
+ *             receives the state after token T-n_slots+j. No state_in[s] may
+ *             point into it: the kernel checks each pointer, leaves that
+ *             sequence unwritten and reports GDN_ERR_DEVICE_ARG through
+ *             gdn_check_device_error.
+ * out         device fp32 [N*T][H][D_v]
+ * n_slots     K >= 1
+ * Returns GDN_OK once the kernel is enqueued on `stream`.
+ */
+gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
+                       const void *v, const float *g, const float *beta,
+                       const float *const *state_in, float *state_slots,
+                       float *out, int n_slots, gdn_mode mode,
+                       gdn_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Varlen chunked prefill ("llama : enable chunked fused GDN path", llama.cpp
+ * commits, tag b9752). Sequence s covers packed tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]). Tokens [0, L_s - n_slots) of each
+ * sequence run through the chunked (chunk 64, WY/UT-transform) tensor-core
+ * kernels, with the last partial chunk padded by no-op rows; the last
+ * n_slots tokens run through the recurrent kernel, which writes the slots.
+ * The result equals the token recurrence up to rounding (bf16 tensor-core
+ * operands, fp32 accumulation and fp32 state).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int n_seqs;         /* N >= 1 */
+  int total_tokens;   /* Ntok = cu_seqlens[N] */
+  int H;
+  int D_k, D_v;       /* D_k = D_v = 128 for the tensor-core path */
+  gdn_dtype in_dtype; /* GDN_BF16 (fp32 inputs use gdn_forward per sequence) */
+  float scale;        /* 0 means 1/sqrt(D_k) */
+} gdn_varlen_shape;
+
+/* Bytes of device workspace gdn_forward_chunked needs for this shape. */
+size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots);
+
+/*
+ * cu_seqlens  device int32 [N+1], non-decreasing, cu_seqlens[0] = 0,
+ *             cu_seqlens[N] = total_tokens (checked on the device)
+ * q, k, v, g, beta, out: as gdn_forward with Ntok = total_tokens
+ * state_in    device array of N device pointers (NULL entry = zero state)
+ * state_slots device fp32 [N][n_slots][H][D_k][D_v]
+ * workspace   device buffer of at least gdn_chunked_workspace_size bytes,
+ *             256-byte aligned; its contents on entry do not matter.
+ */
+gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
+                               const int32_t *cu_seqlens, const void *q,
+                               const void *k, const void *v, const float *g,
+                               const float *beta, const float *const *state_in,
+                               float *state_slots, float *out, int n_slots,
+                               gdn_mode mode, void *workspace,
+                               size_t workspace_bytes, gdn_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Rollback bookkeeping: a host-side table with one entry per sequence (the
+ * recurrent memory's per-sequence record of which stored state is live,
+ * "llama-memory-recurrent: clear rs_idx in clear", koboldcpp commits, tag
+ * v1.113.1). No device work.
+ * ---------------------------------------------------------------------- */
+typedef struct gdn_seq_table gdn_seq_table;
+
+gdn_status gdn_seq_table_create(int n_seqs, int n_slots, gdn_seq_table **out);
+void gdn_seq_table_destroy(gdn_seq_table *table);
+
+/* Records that the last forward ran T_last tokens of sequence `seq`. */
+gdn_status gdn_seq_table_record(gdn_seq_table *table, int seq, int T_last);
+
+/* Forgets the last forward of `seq` (only n_accepted = 0 is valid after). */
+gdn_status gdn_seq_table_clear(gdn_seq_table *table, int seq);
+
+/*
+ * Which state holds sequence `seq` after accepting the first n_accepted
+ * tokens of its last forward: *slot = -1 means "the state_in of that forward
+ * is unchanged"; otherwise the slot index. GDN_ERR_ROLLBACK_RANGE when
+ * n_accepted is outside [0, T_last] or the token was not snapshotted (the
+ * caller must recompute). The table is not modified.
+ */
+gdn_status gdn_rollback(const gdn_seq_table *table, int seq, int n_accepted,
+                        int *slot);
+
+/*
+ * Device address of slot `slot` of sequence `seq` in a state_slots buffer of
+ * the layout above, for building the next call's state_in array. Pure
+ * address arithmetic; *out = NULL for slot = -1.
+ */
+gdn_status gdn_slot_state_ptr(const float *state_slots, int seq, int slot,
+                              int n_slots, int H, int D_k, int D_v,
+                              const float **out);
+
+/* ------------------------------------------------------------------------
+ * Device error word of the current device: synchronises `stream`, then
+ * reads and clears the word. GDN_OK if no kernel reported a problem since
+ * the last check; else GDN_ERR_TIMEOUT or GDN_ERR_DEVICE_ARG with a message.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_check_device_error(gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

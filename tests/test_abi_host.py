@@ -1,0 +1,171 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/gdn.h declares, validates arguments before touching the
+device, and implements the rollback bookkeeping exactly as the oracle's slot
+choice defines it."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_delta_net_02_gb300 import build
+    build.build()
+    from gated_delta_net_02_gb300 import gdn as mod
+    return mod
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(gdn):
+    names = declared_functions()
+    assert "gdn_forward" in names and "gdn_rollback" in names and "gdn_forward_chunked" in names
+    for name in names:
+        assert hasattr(gdn.lib, name), name
+        assert ctypes.cast(getattr(gdn.lib, name), ctypes.c_void_p).value
+
+
+def test_version(gdn):
+    assert "sm_103a" in gdn.gdn_version()
+
+
+def shape(gdn, **kw):
+    base = dict(n_seqs=2, T=3, H=2, D_k=128, D_v=128, in_dtype=gdn.GDN_BF16, scale=0.0)
+    base.update(kw)
+    return gdn.gdn_shape(**base)
+
+
+FAKE = 1 << 20  # 16-byte aligned non-null address; never dereferenced here
+
+
+def call_forward(gdn, sh, n_slots=1, mode="gda", **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=FAKE, state_slots=FAKE,
+             out=FAKE)
+    p.update(ptrs)
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_forward(sh, p["q"], p["k"], p["v"], p["g"], p["beta"], p["state_in"],
+                        p["state_slots"], p["out"], n_slots, mode)
+    return e.value.status
+
+
+def test_forward_argument_errors(gdn):
+    assert call_forward(gdn, shape(gdn, D_k=32)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_forward(gdn, shape(gdn, D_v=96)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_forward(gdn, shape(gdn), n_slots=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, H=0)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, T=-1)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, in_dtype=7)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, scale=float("nan"))) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn), q=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn), beta=FAKE + 4) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn), state_in=0) == gdn.GDN_ERR_INVALID_ARG
+    rc = gdn.lib.gdn_forward(ctypes.byref(shape(gdn)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             FAKE, FAKE, 1, 9, None)
+    assert rc == gdn.GDN_ERR_INVALID_ARG
+    assert "mode" in gdn.gdn_last_error()
+
+
+def test_null_shape(gdn):
+    assert gdn.lib.gdn_forward(None, 0, 0, 0, 0, 0, 0, 0, 0, 1, 0, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(gdn):
+    # no sequences: nothing to validate or launch, no device needed
+    gdn.gdn_forward(shape(gdn, n_seqs=0), 0, 0, 0, 0, 0, 0, 0, 0, 1, "gda")
+
+
+def vshape(gdn, **kw):
+    base = dict(n_seqs=2, total_tokens=100, H=2, D_k=128, D_v=128, in_dtype=gdn.GDN_BF16,
+                scale=0.0)
+    base.update(kw)
+    return gdn.gdn_varlen_shape(**base)
+
+
+def call_chunked(gdn, sh, n_slots=1, ws_bytes=None, **ptrs):
+    p = dict(cu=FAKE, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=FAKE,
+             state_slots=FAKE, out=FAKE, ws=FAKE)
+    p.update(ptrs)
+    if ws_bytes is None:
+        ws_bytes = gdn.gdn_chunked_workspace_size(sh, n_slots)
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_forward_chunked(sh, p["cu"], p["q"], p["k"], p["v"], p["g"], p["beta"],
+                                p["state_in"], p["state_slots"], p["out"], n_slots, "gda",
+                                p["ws"], ws_bytes)
+    return e.value.status
+
+
+def test_chunked_argument_errors(gdn):
+    assert call_chunked(gdn, vshape(gdn, D_k=64, D_v=64)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_chunked(gdn, vshape(gdn, in_dtype=gdn.GDN_F32)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_chunked(gdn, vshape(gdn, n_seqs=0)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn), n_slots=0, ws_bytes=1 << 30) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn), cu=0) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn), ws=FAKE + 16) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn), ws_bytes=1) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn), out=FAKE + 8) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_workspace_size_grows_with_tokens(gdn):
+    a = gdn.gdn_chunked_workspace_size(vshape(gdn, total_tokens=1000), 8)
+    b = gdn.gdn_chunked_workspace_size(vshape(gdn, total_tokens=100000), 8)
+    assert 0 < a <= b
+    assert gdn.gdn_chunked_workspace_size(vshape(gdn), 0) == 0
+
+
+@pytest.mark.parametrize("T,K", [(8, 8), (8, 3), (1, 1), (5, 1), (3, 6), (0, 2)])
+def test_rollback_matches_oracle_slot_choice(gdn, T, K):
+    t = gdn.SeqTable(3, K)
+    t.record(1, T)
+    for n in range(-2, T + 3):
+        try:
+            want = oracle.rollback_slot(T, K, n)
+        except oracle.RollbackRangeError:
+            want = None
+        if want is None:
+            with pytest.raises(gdn.GDNError) as e:
+                t.rollback(1, n)
+            assert e.value.status == gdn.GDN_ERR_ROLLBACK_RANGE
+        else:
+            assert t.rollback(1, n) == want
+    t.close()
+
+
+def test_seq_table_record_clear_and_bounds(gdn):
+    t = gdn.SeqTable(2, 4)
+    assert t.rollback(0, 0) == -1          # never ran: only "keep the input"
+    with pytest.raises(gdn.GDNError):
+        t.rollback(0, 1)
+    t.record(0, 4)
+    assert t.rollback(0, 4) == 3 and t.rollback(0, 1) == 0
+    t.clear(0)                              # a cleared sequence has no slots
+    with pytest.raises(gdn.GDNError) as e:
+        t.rollback(0, 1)
+    assert e.value.status == gdn.GDN_ERR_ROLLBACK_RANGE
+    for bad in [(-1, 0), (2, 0)]:
+        with pytest.raises(gdn.GDNError) as e:
+            t.rollback(*bad)
+        assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+    with pytest.raises(gdn.GDNError):
+        t.record(0, -1)
+    with pytest.raises(gdn.GDNError):
+        gdn.SeqTable(1, 0)
+
+
+def test_slot_state_ptr_arithmetic(gdn):
+    base = 1 << 30
+    H, Dk, Dv, K = 3, 64, 128, 5
+    p = gdn.gdn_slot_state_ptr(base, 2, 4, K, H, Dk, Dv)
+    assert p == base + ((2 * K + 4) * H * Dk * Dv) * 4
+    assert gdn.gdn_slot_state_ptr(base, 2, -1, K, H, Dk, Dv) == 0
+    with pytest.raises(gdn.GDNError):
+        gdn.gdn_slot_state_ptr(base, 0, K, K, H, Dk, Dv)
