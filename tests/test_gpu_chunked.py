@@ -1,0 +1,134 @@
+"""GPU parity of the chunked (tensor-core) prefill against the fp64 oracle,
+through the C ABI: varlen batches with ragged last chunks, sequences shorter
+than one chunk or than K, GDA and KDA, K snapshot slots from the recurrent
+tail, the full-size KDA and varlen workloads, zero-state pointers and a bad
+cu_seqlens table reported by the device."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_net_02_gb300 import inputs
+
+from _helpers import gpu_forward, oracle_run, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 5e-3
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_delta_net_02_gb300 import build
+    build.build()
+    from gated_delta_net_02_gb300 import gdn as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+def chunked_forward(gdn, b, n_slots=None, state_ptrs=None, cu=None, check=True,
+                    dev_tensors=None):
+    n_slots = b.n_slots if n_slots is None else n_slots
+    d = dev_tensors or to_dev(b)
+    N = b.n_seqs
+    H, Dk, Dv = b.q.shape[1], b.q.shape[2], b.v.shape[2]
+    ntok = b.q.shape[0]
+    cu_dev = (b.cu_seqlens if cu is None else cu).to(torch.int32).cuda()
+    shape = gdn.gdn_varlen_shape(N, ntok, H, Dk, Dv, gdn.GDN_BF16, b.scale)
+    ws_bytes = gdn.gdn_chunked_workspace_size(shape, n_slots)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    slots = torch.full((N, n_slots, H, Dk, Dv), float("nan"), device="cuda")
+    out = torch.full((ntok, H, Dv), float("nan"), device="cuda")
+    if state_ptrs is None:
+        state_ptrs = gdn.state_ptr_array(gdn.per_seq_state_ptrs(d["state"], N), "cuda")
+    gdn.gdn_forward_chunked(shape, cu_dev, d["q"], d["k"], d["v"], d["g"], d["beta"], state_ptrs,
+                            slots, out, n_slots, b.mode, ws, ws_bytes)
+    if check:
+        gdn.gdn_check_device_error()
+    return out, slots
+
+
+def compare(b, out, slots, n_slots=None, tol=TOL_BF16):
+    n_slots = b.n_slots if n_slots is None else n_slots
+    o_ref, s_ref, sl_ref = oracle_run(b, n_slots=n_slots)
+    out = out.double().cpu().numpy()
+    slots = slots.double().cpu().numpy()
+    assert not np.isnan(out).any(), "unwritten outputs"
+    e_out = rel_l2(out, o_ref)
+    e_fin = rel_l2(slots[:, -1], s_ref)
+    assert e_out <= tol, f"out rel-L2 {e_out}"
+    assert e_fin <= tol, f"final state rel-L2 {e_fin}"
+    for j in range(n_slots):
+        written = ~np.isnan(sl_ref[:, j, 0, 0, 0])
+        if written.any():
+            e = rel_l2(slots[written, j], sl_ref[written, j])
+            assert e <= tol, f"slot {j} rel-L2 {e}"
+        assert np.isnan(slots[~written, j]).all()
+    return e_out, e_fin
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+def test_varlen_ragged_small(gdn, mode):
+    # chunk-multiple, ragged, one-chunk, shorter-than-K and empty sequences
+    lens = [200, 64, 131, 9, 1, 0, 65]
+    b = inputs.make_batch(41, lens, 2, 128, 128, mode=mode, n_slots=4)
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("K", [1, 8])
+def test_single_long_sequence(gdn, mode, K):
+    b = inputs.make_batch(42 + K, [777], 3, 128, 128, mode=mode, n_slots=K)
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)
+
+
+def test_kda_prefill_full_size(gdn):
+    """1 sequence, T=4096, H=32, D=128, KDA gate, bf16 q/k/v, K=1, seed 3."""
+    b = inputs.kda_prefill(3)
+    out, slots = chunked_forward(gdn, b)
+    e_out, e_fin = compare(b, out, slots)
+    print(f"kda prefill: out rel-L2 {e_out:.2e}, state rel-L2 {e_fin:.2e}")
+
+
+def test_varlen_prefill_full_size(gdn):
+    """8 sequences, lengths ~U[512, 8192], H=16, D=128, GDA, K=8, seed 4."""
+    b = inputs.varlen_prefill(4)
+    out, slots = chunked_forward(gdn, b)
+    e_out, e_fin = compare(b, out, slots)
+    print(f"varlen prefill: out rel-L2 {e_out:.2e}, state rel-L2 {e_fin:.2e}")
+
+
+def test_matches_recurrent_path(gdn):
+    b = inputs.make_batch(43, [300, 300], 2, 128, 128, mode="gda", n_slots=2)
+    out_c, sl_c = chunked_forward(gdn, b)
+    out_r, sl_r = gpu_forward(b)
+    assert rel_l2(out_c.double().cpu().numpy(), out_r.double().cpu().numpy()) < TOL_BF16
+    assert rel_l2(sl_c.double().cpu().numpy(), sl_r.double().cpu().numpy()) < TOL_BF16
+
+
+def test_zero_state_pointers(gdn):
+    b = inputs.make_batch(44, [150, 70], 2, 128, 128, state_std=0.0, n_slots=2)
+    out_a, sl_a = chunked_forward(gdn, b)
+    ptrs = gdn.state_ptr_array([0, 0], "cuda")
+    out_b, sl_b = chunked_forward(gdn, b, state_ptrs=ptrs)
+    assert torch.equal(out_a, out_b) and torch.equal(sl_a, sl_b)
+
+
+def test_bad_cu_seqlens_reported_by_device(gdn):
+    b = inputs.make_batch(45, [100, 50], 2, 128, 128, n_slots=1)
+    bad = torch.tensor([0, 120, 150], dtype=torch.int64)   # non-matching split is fine
+    chunked_forward(gdn, b, cu=bad)                           # valid table: no error
+    for cu in ([0, 160, 150], [5, 100, 150], [0, 100, 149]):
+        chunked_forward(gdn, b, cu=torch.tensor(cu), check=False)
+        with pytest.raises(gdn.GDNError) as e:
+            gdn.gdn_check_device_error()
+        assert e.value.status == gdn.GDN_ERR_DEVICE_ARG
+    gdn.gdn_check_device_error()
+
+
+def test_repeated_calls_reuse_dirty_workspace(gdn):
+    b = inputs.make_batch(46, [257, 90], 2, 128, 128, mode="kda", n_slots=3)
+    out1, sl1 = chunked_forward(gdn, b)
+    out2, sl2 = chunked_forward(gdn, b)
+    assert torch.equal(out1, out2) and torch.equal(sl1, sl2)
