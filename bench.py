@@ -165,10 +165,11 @@ def timed_graph_steps(graphs, K, stream):
     assert left == 0, "graph plan does not cover K"
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for g in plan:
-        g.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        start.record(stream)
+        for g in plan:
+            g.replay()
+        end.record(stream)
     end.synchronize()
     return start.elapsed_time(end)
 
@@ -347,7 +348,126 @@ class Verify(Decode):
         return run
 
 
-WORKLOADS = {"decode": Decode, "verify": Verify}
+class Prefill:
+    """Chunked prefill through gdn_forward_chunked; one step = one call."""
+    name = "prefill"
+    SETS = 2        # rotating input sets, each larger than half the L2
+    mode = "gda"
+
+    def batch(self, j):
+        raise NotImplementedError
+
+    def setup(self, gdn, dev):
+        self.gdn = gdn
+        self.sets = []
+        for j in range(self.SETS):
+            b = self.batch(j)
+            d = {n: getattr(b, n).to(dev) for n in ("q", "k", "v", "g", "beta", "state")}
+            d["cu"] = b.cu_seqlens.to(torch.int32).to(dev)
+            d["ptrs"] = gdn.state_ptr_array(gdn.per_seq_state_ptrs(d["state"], b.n_seqs), dev)
+            self.sets.append((b, d))
+        b0 = self.sets[0][0]
+        self.b0 = b0
+        self.N, self.H = b0.n_seqs, b0.q.shape[1]
+        self.ntok = b0.q.shape[0]
+        self.K = b0.n_slots
+        self.shape = gdn.gdn_varlen_shape(self.N, self.ntok, self.H, 128, 128, gdn.GDN_BF16,
+                                          b0.scale)
+        self.ws_bytes = gdn.gdn_chunked_workspace_size(self.shape, self.K)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.slots = torch.empty(self.N, self.K, self.H, 128, 128, device=dev)
+        self.out = torch.empty(self.ntok, self.H, 128, device=dev)
+        self.pinned = [getattr(b0, n).pin_memory() for n in ("q", "k", "v", "g", "beta")]
+        self.stage = [t.to(dev) for t in self.pinned]
+        self.out_host = torch.empty(self.ntok, self.H, 128).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.pinned)
+        self.d2h_bytes = self.out.numel() * 4
+
+    @property
+    def tokens_per_step(self):
+        return self.ntok
+
+    def alg_bytes_per_step(self):
+        g_bytes = 4 * 128 if self.mode == "kda" else 4
+        per_tok_head = 3 * 128 * 2 + g_bytes + 4 + 4 * 128
+        state = 2 * self.N * self.H * 128 * 128 * 4 + self.N * self.K * self.H * 128 * 128 * 4
+        return per_tok_head * self.ntok * self.H + state
+
+    def alg_flops_per_step(self):
+        C, D = 64, 128
+        return (2 * C * (3 * D + 2 * D) + 6 * D * D) * self.ntok * self.H
+
+    def _call(self, d, q, k, v, g, beta, stream):
+        self.gdn.gdn_forward_chunked(self.shape, d["cu"], q, k, v, g, beta, d["ptrs"],
+                                     self.slots, self.out, self.K, self.mode, self.ws,
+                                     self.ws_bytes, stream)
+
+    def step(self, i, stream):
+        _, d = self.sets[i % self.SETS]
+        self._call(d, d["q"], d["k"], d["v"], d["g"], d["beta"], stream)
+
+    def step_e2e(self, i, stream):
+        for st, h in zip(self.stage, self.pinned):
+            st.copy_(h, non_blocking=True)
+        _, d = self.sets[0]
+        q, k, v, g, beta = self.stage
+        self._call(d, q, k, v, g, beta, stream)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def graph_len(self):
+        return 4
+
+    def oracle_step_fn(self, n_seqs):
+        import oracle
+        b = self.batch(0)
+        cu = b.cu_seqlens
+        self.ntok, self.H, self.K = b.q.shape[0], b.q.shape[1], b.n_slots
+        H = max(1, min(self.H, n_seqs))   # bounded sample: a subset of the heads
+        args = [inputs.to_f64(getattr(b, n)[:, :H]) for n in ("q", "k", "v", "g", "beta")]
+        S0 = inputs.to_f64(b.state[:, :H])
+
+        def run():
+            oracle.forward(*args, S0, mode=self.mode, scale=b.scale, n_slots=self.K,
+                           seq_start=cu[:-1].numpy(), seq_len=b.seq_len.numpy())
+            return self.ntok * H / self.H
+        return run
+
+
+class PrefillKDA(Prefill):
+    name = "prefill_kda"
+    mode = "kda"
+    N = 1
+
+    def batch(self, j):
+        return inputs.kda_prefill(3 + 100 * j)
+
+    def config(self):
+        return {"workload": "KDA per-row-gate chunked prefill: 1 sequence x T=4096, H=32, "
+                            "D_k=D_v=128, bf16 q/k/v, fp32 g [T,H,D_k] and state, K=1",
+                "tokens_per_step": 4096, "heads": 32, "chunk": 64,
+                "l2": "inputs larger than L2: 2 rotating input sets of 240 MB",
+                "timing": "CUDA graphs of consecutive calls, CUDA events on the launch stream"}
+
+
+class PrefillVarlen(Prefill):
+    name = "prefill_varlen"
+    mode = "gda"
+    N = 8
+
+    def batch(self, j):
+        return inputs.varlen_prefill(4 + 100 * j)
+
+    def config(self):
+        return {"workload": "varlen GDA chunked prefill: 8 sequences, lengths ~U[512,8192] "
+                            "(seed 4), H=16, D_k=D_v=128, bf16 q/k/v, fp32 state, K=8 slots",
+                "tokens_per_step": int(inputs.varlen_lengths(4).sum()), "heads": 16,
+                "chunk": 64,
+                "l2": "inputs larger than L2: 2 rotating input sets",
+                "timing": "CUDA graphs of consecutive calls, CUDA events on the launch stream"}
+
+
+WORKLOADS = {"decode": Decode, "verify": Verify, "prefill_kda": PrefillKDA,
+             "prefill_varlen": PrefillVarlen}
 
 
 # ----------------------------------------------------------------- arms
@@ -450,8 +570,9 @@ def gdn_arm(args, wl_cls):
     stream.synchronize()
     gdn.gdn_check_device_error(stream)
     graphs = graphs_for(wl.step)
-    for g, _ in graphs:  # one untimed replay uploads each graph
-        g.replay()
+    with torch.cuda.stream(stream):
+        for g, _ in graphs:  # one untimed replay uploads each graph
+            g.replay()
     stream.synchronize()
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -467,8 +588,9 @@ def gdn_arm(args, wl_cls):
 
     # e2e: host tokens in, host outputs back, per step, same K
     graphs_e2e = graphs_for(wl.step_e2e)
-    for g, _ in graphs_e2e:
-        g.replay()
+    with torch.cuda.stream(stream):
+        for g, _ in graphs_e2e:
+            g.replay()
     stream.synchronize()
     barrier()
     ms_e2e = timed_graph_steps(graphs_e2e, K, stream)
@@ -489,21 +611,37 @@ def gdn_arm(args, wl_cls):
         hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         kern_s = ms / K / 1e3  # this rank's average launch duration
         achieved = wl.alg_bytes_per_step() / kern_s / 1e9
-        sha = source_sha("recurrent.cu", "common.cuh")
+        if isinstance(wl, Prefill):
+            sha = source_sha("chunked.cu", "umma.cuh", "common.cuh")
+            tflops = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+            flops = wl.alg_flops_per_step() / kern_s / 1e12
+            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm,
+                    "traffic": ncu_traffic("gdn_chunked_" + wl.name, sha),
+                    "kernel": "whole gdn_forward_chunked call (work list, chunk prep, "
+                              "chunk scan, recurrent tail)",
+                    "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
+                    "tensor": {"achieved": flops, "peak": tflops, "unit": "TFLOP/s",
+                               "frac": flops / tflops,
+                               "algorithmic_flops_per_launch": wl.alg_flops_per_step()},
+                    "peak_source": f"{src} hbm_gbs and bf16_tflops"}
+        else:
+            sha = source_sha("recurrent.cu", "common.cuh")
+            roof = None
         traffic = ncu_traffic("gdn_recurrent_" + wl.name, sha)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_max / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": wl.config(),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": traffic,
-                         "kernel": "recurrent_kernel (gdn_forward)",
-                         "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
-                         "peak_source": f"{src} hbm_gbs"},
+            "roofline": roof or {"bound": "hbm", "achieved": achieved, "peak": hbm,
+                                 "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                                 "kernel": "recurrent_kernel (gdn_forward)",
+                                 "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
+                                 "peak_source": f"{src} hbm_gbs"},
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-            "gpu_launches": K,
+            "gpu_launches": K * (4 if isinstance(wl, Prefill) else 1),
             "clocks": summarize_clocks(clock_rows, t_wall0, t_wall1),
         }
         if not args.no_cpu_baseline:
