@@ -186,10 +186,15 @@ def capture(fn_steps, stream, steps):
 # ----------------------------------------------------------------- workloads
 
 class Decode:
-    """64 sequences x 1 token, H=16, D=128, GDA, bf16 q/k/v, fp32 state."""
+    """64 sequences x 1 token, H=16, D=128, GDA, bf16 q/k/v, fp32 state.
+
+    Cold-L2 protocol: SETS independent decode batches, each with its own
+    double-buffered state; step i advances batch i % SETS, so between two
+    steps of one batch the other batches move (SETS-1) x 128 MiB through
+    the memory system and its state is read from HBM, not L2."""
     N, H, D = 64, 16, 128
     POOL = 256      # distinct token steps resident on the device
-    BANKS = 8       # rotating state banks (8 x 64 MiB = 512 MiB > 3 x L2)
+    SETS = 8        # independent batches (8 x 2 x 64 MiB = 1 GiB)
     name = "decode"
 
     @property
@@ -201,8 +206,9 @@ class Decode:
                             "scalar gate, bf16 q/k/v, fp32 state ~N(0,0.05), K=1 slot",
                 "n_seqs": self.N, "heads": self.H, "D_k": self.D, "D_v": self.D,
                 "tokens_per_step": self.N, "input_dtype": "bf16", "state_dtype": "f32",
-                "l2": f"inputs larger than L2: the state chain rotates over {self.BANKS} "
-                      f"banks of 64 MiB and {self.POOL} distinct token steps",
+                "l2": f"inputs larger than L2: {self.SETS} independent 64-sequence decode "
+                      f"batches advance in turn (each step's 64 MiB state was last written "
+                      f"{self.SETS - 1} steps earlier), {self.POOL} distinct token steps",
                 "timing": "CUDA graphs of consecutive steps, CUDA events on the launch stream"}
 
     def alg_bytes_per_step(self):
@@ -213,11 +219,11 @@ class Decode:
     def setup(self, gdn, dev):
         N, H, D = self.N, self.H, self.D
         self.gdn = gdn
-        self.banks = [inputs.decode_state(1, N, H, D).to(dev) for _ in range(1)]
-        for _ in range(self.BANKS - 1):
-            self.banks.append(torch.empty_like(self.banks[0]))
-        self.bank_ptrs = [gdn.state_ptr_array(gdn.per_seq_state_ptrs(b, N), dev)
-                          for b in self.banks]
+        s0 = inputs.decode_state(1, N, H, D).to(dev)
+        self.bufs = [[s0.clone(), torch.empty_like(s0)] for _ in range(self.SETS)]
+        del s0
+        self.buf_ptrs = [[gdn.state_ptr_array(gdn.per_seq_state_ptrs(b, N), dev) for b in pair]
+                         for pair in self.bufs]
         toks = [inputs.decode_tokens(1, s, N, H, D) for s in range(self.POOL)]
         self.host = [torch.stack([t[i] for t in toks]) for i in range(5)]  # q,k,v,g,beta
         self.dev = [h.to(dev) for h in self.host]
@@ -230,27 +236,32 @@ class Decode:
         self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
         self.d2h_bytes = self.out.numel() * 4
 
+    def _bufs(self, i):
+        """(state_in pointer array, slot buffer) of step i: batch i % SETS,
+        ping-ponging between its two state buffers."""
+        b = i % self.SETS
+        parity = (i // self.SETS) % 2
+        return self.buf_ptrs[b][parity], self.bufs[b][1 - parity]
+
     def step(self, i, stream):
         p = i % self.POOL
-        src = i % self.BANKS
-        dst = (i + 1) % self.BANKS
+        src, dst = self._bufs(i)
         q, k, v, g, beta = (t[p] for t in self.dev)
-        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[src],
-                             self.banks[dst], self.out, 1, "gda", stream)
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, self.out, 1, "gda",
+                             stream)
 
     def step_e2e(self, i, stream):
         p = i % self.POOL
         for s, h in zip(self.stage, self.pinned):
             s.copy_(h[p], non_blocking=True)
-        src = i % self.BANKS
-        dst = (i + 1) % self.BANKS
+        src, dst = self._bufs(i)
         q, k, v, g, beta = self.stage
-        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[src],
-                             self.banks[dst], self.out, 1, "gda", stream)
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, self.out, 1, "gda",
+                             stream)
         self.out_host.copy_(self.out, non_blocking=True)
 
     def graph_len(self):
-        return self.POOL  # a multiple of BANKS: replays continue the chain
+        return self.POOL  # a multiple of 2 x SETS: replays continue every chain
 
     # ---- CPU oracle on a bounded sample of the same workload
     def oracle_step_fn(self, n_seqs):
