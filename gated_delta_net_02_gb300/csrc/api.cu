@@ -213,6 +213,77 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
                       "gdn_forward_chunked launch");
 }
 
+// Same computation as gdn_forward_chunked, but the scratch it needs lives in
+// a fixed device array inside the library instead of a caller workspace, so
+// the call allocates nothing. For callers that cannot allocate device memory
+// themselves (hosts that own every byte through their own pool, loops that
+// must not pay for a device allocation).
+gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
+                                       const int32_t *cu_seqlens, const void *q,
+                                       const void *k, const void *v, const float *g,
+                                       const float *beta, const float *const *state_in,
+                                       float *state_slots, float *out, int n_slots,
+                                       gdn_mode mode, gdn_stream_t stream) {
+  const char *fn = "gdn_forward_chunked_noalloc";
+  if (!shape) return fail(GDN_ERR_INVALID_ARG, "%s: shape is NULL", fn);
+  const gdn_varlen_shape &s = *shape;
+  if (s.n_seqs <= 0 || s.total_tokens < 0 || s.H <= 0)
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs=%d total_tokens=%d H=%d", fn, s.n_seqs,
+                s.total_tokens, s.H);
+  if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
+    return fail(GDN_ERR_INVALID_ARG, "%s: mode %d", fn, (int)mode);
+  if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
+    return fail(GDN_ERR_INVALID_ARG, "%s: in_dtype %d", fn, (int)s.in_dtype);
+  if (n_slots < 1) return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d (need >= 1)", fn, n_slots);
+  if (s.D_k != 128 || s.D_v != 128)
+    return fail(GDN_ERR_UNSUPPORTED, "%s: tensor-core path needs D_k = D_v = 128 (got %d, %d)",
+                fn, s.D_k, s.D_v);
+  if (s.in_dtype != GDN_BF16)
+    return fail(GDN_ERR_UNSUPPORTED, "%s: bf16 inputs only (fp32 inputs: use gdn_forward)", fn);
+  if (!std::isfinite(s.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+  if ((long long)s.total_tokens * s.H > (1LL << 31))
+    return fail(GDN_ERR_UNSUPPORTED, "%s: too many token-heads", fn);
+  const void *ptrs[] = {cu_seqlens, state_in, state_slots};
+  const char *names[] = {"cu_seqlens", "state_in", "state_slots"};
+  for (int i = 0; i < 3; ++i)
+    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
+  if (s.total_tokens > 0) {
+    const void *tp[] = {q, k, v, g, beta, out};
+    const char *tn[] = {"q", "k", "v", "g", "beta", "out"};
+    for (int i = 0; i < 6; ++i) {
+      if (!tp[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, tn[i]);
+      if (!aligned16(tp[i]))
+        return fail(GDN_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, tn[i]);
+    }
+  }
+  if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
+    return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
+  const size_t need = gdn_chunked_workspace_size(shape, n_slots);
+  if (need > gdn::static_scratch_bytes())
+    return fail(GDN_ERR_UNSUPPORTED,
+                "%s: this shape needs %zu bytes of scratch; the built-in area holds %zu "
+                "(use gdn_forward_chunked with a workspace)",
+                fn, need, gdn::static_scratch_bytes());
+  int *err = nullptr;
+  gdn_status st = device_err_ptr(&err);
+  if (st != GDN_OK) return st;
+
+  gdn::ChunkedArgs a{};
+  a.cu_seqlens = cu_seqlens;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state_in = state_in; a.slots = state_slots; a.out = out;
+  a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
+  a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
+  a.kda = mode == GDN_MODE_KDA;
+  a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
+  a.err = err;
+  size_t need2 = 0;
+  return check_launch(
+      gdn::launch_chunked_static(a, reinterpret_cast<cudaStream_t>(stream), &need2), fn);
+}
+
+size_t gdn_noalloc_scratch_bytes(void) { return gdn::static_scratch_bytes(); }
+
 // ---- rollback table --------------------------------------------------------
 
 struct gdn_seq_table {

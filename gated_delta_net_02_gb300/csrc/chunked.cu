@@ -945,3 +945,52 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace gdn
+
+// ---- allocation-free variant (gdn_forward_chunked_noalloc) -----------------------
+//
+// Some callers cannot hand this library a workspace: code that runs inside a
+// host application which owns all device memory through its own pool, or
+// latency-critical loops where a cudaMalloc (which may synchronise the whole
+// device) is not acceptable. For them the chunked path can run from a fixed
+// scratch area compiled into the library. It is a plain device array, so
+// every GPU that loads this library's chunked kernels keeps it (64 MiB)
+// until the process exits.
+namespace gdn {
+
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64] = {};
+}  // namespace
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// *need = workspace bytes this shape needs. Returns cudaErrorInvalidValue
+// (and launches nothing) when *need exceeds the static area. The first call
+// on a device looks up the area's device address with that device current.
+cudaError_t launch_chunked_static(ChunkedArgs a, cudaStream_t stream, size_t *need) {
+  *need = chunked_workspace_size(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.n_slots);
+  if (*need > kStaticScratchBytes) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void *base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_addr[dev] = p;
+    }
+    base = g_scratch_addr[dev];
+  }
+  a.workspace = base;
+  a.workspace_bytes = kStaticScratchBytes;
+  return launch_chunked(a, stream);
+}
+
+}  // namespace gdn

@@ -45,4 +45,9 @@ size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk,
                               int Dv, int n_slots);
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream);
 
+// The chunked path on the library's fixed scratch area (no workspace
+// argument); see gdn_forward_chunked_noalloc in gdn.h.
+size_t static_scratch_bytes();
+cudaError_t launch_chunked_static(ChunkedArgs a, cudaStream_t stream, size_t *need);
+
 }  // namespace gdn

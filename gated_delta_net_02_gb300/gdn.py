@@ -67,6 +67,11 @@ lib.gdn_forward_chunked.restype = _st
 lib.gdn_forward_chunked.argtypes = [ctypes.POINTER(gdn_varlen_shape), _vp, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, ctypes.c_size_t,
                                     _vp]
+lib.gdn_forward_chunked_noalloc.restype = _st
+lib.gdn_forward_chunked_noalloc.argtypes = [ctypes.POINTER(gdn_varlen_shape), _vp, _vp, _vp,
+                                            _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]
+lib.gdn_noalloc_scratch_bytes.restype = ctypes.c_size_t
+lib.gdn_noalloc_scratch_bytes.argtypes = []
 lib.gdn_seq_table_create.restype = _st
 lib.gdn_seq_table_create.argtypes = [_i, _i, ctypes.POINTER(_vp)]
 lib.gdn_seq_table_destroy.restype = None
@@ -133,6 +138,21 @@ def gdn_forward_chunked(shape: gdn_varlen_shape, cu_seqlens, q, k, v, g, beta, s
                                    _addr(state_in), _addr(state_slots), _addr(out),
                                    int(n_slots), _MODES[mode], _addr(workspace),
                                    int(workspace_bytes), _stream(stream)))
+
+
+def gdn_forward_chunked_noalloc(shape: gdn_varlen_shape, cu_seqlens, q, k, v, g, beta,
+                                state_in, state_slots, out, n_slots: int, mode,
+                                stream=None) -> None:
+    """gdn_forward_chunked without a workspace: the library's built-in
+    scratch array is used (for callers that cannot allocate device memory)."""
+    _check(lib.gdn_forward_chunked_noalloc(ctypes.byref(shape), _addr(cu_seqlens), _addr(q),
+                                           _addr(k), _addr(v), _addr(g), _addr(beta),
+                                           _addr(state_in), _addr(state_slots), _addr(out),
+                                           int(n_slots), _MODES[mode], _stream(stream)))
+
+
+def gdn_noalloc_scratch_bytes() -> int:
+    return int(lib.gdn_noalloc_scratch_bytes())
 
 
 def gdn_check_device_error(stream=None) -> None:

@@ -149,6 +149,38 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
                                size_t workspace_bytes, gdn_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free chunked prefill. The pages describe no counterpart: this is
+ * a convenience of this library. Some callers cannot give the chunked call a
+ * workspace because they may not allocate device memory at all: a host
+ * application that owns every device byte through its own pool, or a loop
+ * that must never pay for a device allocation (cudaMalloc can synchronise the
+ * whole device). This entry point computes exactly what gdn_forward_chunked
+ * computes, with the same arguments minus the workspace; its scratch is a
+ * fixed 64 MiB device array inside the library, which every GPU that loads
+ * the chunked kernels holds until the process exits.
+ *  - Limit: shapes whose gdn_chunked_workspace_size exceeds
+ *    gdn_noalloc_scratch_bytes() are rejected with GDN_ERR_UNSUPPORTED and a
+ *    message naming both sizes (e.g. 1 x 4096 tokens x 32 heads needs about
+ *    36 MB and fits; 8 x ~4k tokens x 16 heads does not).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the previous
+ *    call's contents; nothing in it needs to start at zero (the work list
+ *    rewrites what the later kernels read). Calls that can overlap on the
+ *    GPU (different streams without ordering) race on it: serialise them.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
+                                       const int32_t *cu_seqlens, const void *q,
+                                       const void *k, const void *v, const float *g,
+                                       const float *beta, const float *const *state_in,
+                                       float *state_slots, float *out, int n_slots,
+                                       gdn_mode mode, gdn_stream_t stream);
+
+/* Size in bytes of the built-in scratch array of gdn_forward_chunked_noalloc. */
+size_t gdn_noalloc_scratch_bytes(void);
+
+/* ------------------------------------------------------------------------
  * Rollback bookkeeping: a host-side table with one entry per sequence (the
  * recurrent memory's per-sequence record of which stored state is live,
  * "llama-memory-recurrent: clear rs_idx in clear", koboldcpp commits, tag
