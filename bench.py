@@ -466,7 +466,10 @@ class PrefillVarlen(Prefill):
     N = 8
 
     def batch(self, j):
-        return inputs.varlen_prefill(4 + 100 * j)
+        # every set keeps the lengths drawn with seed 4; values differ per set
+        lens = inputs.varlen_lengths(4)
+        return inputs.make_batch(5 + 100 * j, lens, 16, 128, 128, mode="gda",
+                                 state_std=0.05, n_slots=8)
 
     def config(self):
         return {"workload": "varlen GDA chunked prefill: 8 sequences, lengths ~U[512,8192] "
