@@ -258,7 +258,8 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   }
   if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
     return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
-  const size_t need = gdn_chunked_workspace_size(shape, n_slots);
+  const size_t need = gdn::chunked_workspace_need(s.n_seqs, s.total_tokens, s.H, s.D_k,
+                                                  s.D_v, mode == GDN_MODE_KDA);
   if (need > gdn::static_scratch_bytes())
     return fail(GDN_ERR_UNSUPPORTED,
                 "%s: this shape needs %zu bytes of scratch; the built-in area holds %zu "
@@ -380,9 +381,11 @@ gdn_status gdn_check_device_error(gdn_stream_t stream) {
   e = cudaMemcpyToSymbol(g_gdn_err_word, &zero, sizeof(int));
   if (e != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn_check_device_error: %s", cudaGetErrorString(e));
-  switch (word) {
+  switch (word & 0xff) {
     case gdn::kDevTimeout:
-      return fail(GDN_ERR_TIMEOUT, "a device-side wait ran out (kernel abandoned its work)");
+      return fail(GDN_ERR_TIMEOUT,
+                  "a device-side wait ran out (kernel abandoned its work; site %d, chunk %d)",
+                  (word >> 8) & 0xff, (word >> 16) & 0x7fff);
     case gdn::kDevBadSeqlens:
       return fail(GDN_ERR_DEVICE_ARG, "cu_seqlens is not a valid offset table");
     case gdn::kDevOverlap:

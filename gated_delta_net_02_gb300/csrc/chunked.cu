@@ -21,14 +21,19 @@
 // Three kernels run per call, all on the caller's stream:
 //  1. worklist_kernel: validates cu_seqlens and lays out the chunks of every
 //     sequence's chunked part [0, L_s - K) plus the K-token tails.
-//  2. chunk_prep_kernel (one CTA per chunk and head, fully parallel):
-//     G = [K; Q] K^T on the tensor cores (tcgen05, accumulator in TMEM),
-//     then A and P with their decays, then T by forward substitution in
-//     fp32; T and P are stored as bf16 in the workspace.
-//  3. chunk_scan_kernel (one CTA per sequence and head, sequential over the
-//     chunks): W^T = (e^g.K)^T T^T, then [D; Q^S0] = [-W; Q^] S0 + [T; 0] V,
-//     then S = e^gC.S0 + K~^T D~ and O += [0; P] D, all on tcgen05 with the
-//     fp32 master state in registers and bf16 copies as MMA operands.
+//  2. chunk_prep_kernel (one CTA per chunk and head, fully parallel): all
+//     the state-independent work of a chunk. G = [K^; Q^] K~^T on the tensor
+//     cores (tcgen05, accumulator in TMEM) gives A and P; T comes from a
+//     blocked fp32 inverse; W = [T'; 0] K is a second tcgen05 product (T' =
+//     T diag(e^g) and raw K for GDA; T and K^ = e^g . K for KDA). T, P and -W
+//     go to the workspace as bf16, and for KDA also Q^ = e^g . Q,
+//     K~ = e^(gC - g) . K and e^gC.
+//  3. chunk_scan_kernel (one CTA per sequence, head and half of the value
+//     columns, sequential over the chunks): only the state-dependent chain,
+//     [D; Q^ S0] = [-W; Q^] S0 + [T; 0] V, then S = e^gC . S0 + K~^T D~ and
+//     O = Q^ S0 + [0; P] D on tcgen05, with the fp32 master state in
+//     registers and a bf16 copy as the MMA operand; the next chunk's tiles
+//     stream in by TMA meanwhile.
 // The last K tokens of each sequence then run through the recurrent kernel,
 // which writes the snapshot slots.
 #include <cuda.h>
@@ -46,18 +51,22 @@ namespace {
 constexpr int CH = 64;  // chunk length
 
 // ---- workspace layout --------------------------------------------------------
+//
+// Per (chunk, head) tiles, bf16 row-major: T and P [64][64], -W [64][128];
+// KDA adds Q^ and K~ [64][128] and e^gC fp32 [128].
 
 struct WsLayout {
   size_t hdr, chunk_seq, chunk_tok, chunk_len, seq_chunk0, seq_nch, tail_start,
-      tail_len, order, state_ptrs, states, T, P, total;
+      tail_len, order, state_ptrs, states, T, P, W, Qh, Kt, gC, total;
   long long max_chunks;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv) {
+WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda) {
   WsLayout w{};
   w.max_chunks = (long long)total_tokens / CH + n_seqs;
+  const size_t tiles = (size_t)w.max_chunks * H;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -75,8 +84,12 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv) {
   w.order = take(sizeof(int) * (size_t)n_seqs);
   w.state_ptrs = take(sizeof(float *) * (size_t)n_seqs);
   w.states = take(sizeof(float) * (size_t)n_seqs * H * Dk * Dv);
-  w.T = take(2 * (size_t)w.max_chunks * H * CH * CH);
-  w.P = take(2 * (size_t)w.max_chunks * H * CH * CH);
+  w.T = take(2 * tiles * CH * CH);
+  w.P = take(2 * tiles * CH * CH);
+  w.W = take(2 * tiles * CH * Dk);
+  w.Qh = kda ? take(2 * tiles * CH * Dk) : w.W;
+  w.Kt = kda ? take(2 * tiles * CH * Dk) : w.W;
+  w.gC = kda ? take(4 * tiles * Dk) : w.W;
   w.total = off;
   return w;
 }
@@ -86,7 +99,8 @@ struct WsPtrs {
       *tail_len, *order;
   const float **state_ptrs;
   float *states;
-  __nv_bfloat16 *T, *P;
+  __nv_bfloat16 *T, *P, *W, *Qh, *Kt;
+  float *gC;
 };
 
 WsPtrs ws_ptrs(void *base, const WsLayout &w) {
@@ -105,7 +119,37 @@ WsPtrs ws_ptrs(void *base, const WsLayout &w) {
   p.states = reinterpret_cast<float *>(b + w.states);
   p.T = reinterpret_cast<__nv_bfloat16 *>(b + w.T);
   p.P = reinterpret_cast<__nv_bfloat16 *>(b + w.P);
+  p.W = reinterpret_cast<__nv_bfloat16 *>(b + w.W);
+  p.Qh = reinterpret_cast<__nv_bfloat16 *>(b + w.Qh);
+  p.Kt = reinterpret_cast<__nv_bfloat16 *>(b + w.Kt);
+  p.gC = reinterpret_cast<float *>(b + w.gC);
   return p;
+}
+
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+  return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+}
+
+// Byte offset of 16-byte chunk cj (8 bf16) of row `row` in a tile of
+// 128-byte swizzled rows.
+__device__ __forceinline__ uint32_t chunk16(int row, int cj) {
+  return (uint32_t)(row * 128 + ((cj ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 pack8(const float *x) {
+  uint4 u;
+  u.x = pack_bf16(x[0], x[1]);
+  u.y = pack_bf16(x[2], x[3]);
+  u.z = pack_bf16(x[4], x[5]);
+  u.w = pack_bf16(x[6], x[7]);
+  return u;
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float *x) {
+  const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = __bfloat162float(b[k]);
 }
 
 // ---- 1. work list ---------------------------------------------------------------
@@ -197,105 +241,148 @@ __global__ void __launch_bounds__(WL_THREADS)
   }
 }
 
-// ---- 2. chunk preparation: T = (I + A)^-1 diag(beta) and P ------------------
+// ---- 2. chunk preparation (all state-independent products) -------------------
 
 constexpr int PREP_THREADS = 128;
 constexpr int AF_LD = 68;  // fp32 row stride of A in shared memory (16-byte rows)
-// shared memory: KQ [128 x 128] bf16 (2 swizzled atom columns of 16 KB),
-// KB [64 x 128] bf16 (KDA B operand), A fp32 [64][AF_LD], gamma, beta, barrier
+// Shared memory, offsets from a 1024-aligned base:
+//  KQ [128][128] bf16: K rows 0..63, Q rows 64..127 (TMA; KDA scales them in
+//     place to K^ = e^g . K and Q^ = e^g . Q). A of G; its K rows are B of W.
+//  KB [64][128] bf16: KDA e^-g . K (B of G); afterwards the fp32 inverse X.
+//  AF [64][AF_LD] fp32: A.   TZ [128][64] bf16: [T'; 0], A of W.
 constexpr int PREP_KQ = 0, PREP_KB = 32768, PREP_AF = 49152;
-constexpr int PREP_GAM = PREP_AF + 64 * AF_LD * 4, PREP_BETA = PREP_GAM + 256;
-constexpr int PREP_BAR = PREP_BETA + 256, PREP_TSLOT = PREP_BAR + 8;
-constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;  // + alignment slack
-
-__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
-  return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-}
+constexpr int PREP_TZ = PREP_AF + 64 * AF_LD * 4;  // 1024-aligned
+constexpr int PREP_YS = PREP_TZ + 16384;           // [3][16][16] f32 level products
+constexpr int PREP_GAM = PREP_YS + 3072;           // [64] f32 gamma (GDA)
+constexpr int PREP_TF = PREP_GAM + 256;            // [64] f32 column factor of T'
+constexpr int PREP_BETA = PREP_TF + 256;           // [64] f32
+constexpr int PREP_BAR = PREP_BETA + 256;          // 3 mbarriers
+constexpr int PREP_TSLOT = PREP_BAR + 24;
+constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;   // + alignment slack
+constexpr uint32_t PCOL_G = 0, PCOL_W = 64;        // TMEM columns (256 allocated)
+static_assert(PREP_TZ % 1024 == 0, "TZ holds swizzled atoms");
 
 // One CTA per (chunk, head). Rows r of the chunk are tokens chunk_tok + r,
 // r < len; the rest are padding (k = q = 0, beta = 0, g = 0).
 template <bool KDA>
 __global__ void __launch_bounds__(PREP_THREADS)
-    chunk_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                      const float *__restrict__ g, const float *__restrict__ beta, int H,
-                      WsPtrs w, int *err) {
+    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
+                      const float *__restrict__ beta, int H, WsPtrs w, int *err) {
   constexpr int DK = 128;
   const int c = blockIdx.x / H, h = blockIdx.x % H;
   if (c >= w.hdr[0]) return;
   const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
+  const long long tile = (long long)c * H + h;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
-  unsigned char *KQ = sm + PREP_KQ, *KB = sm + PREP_KB;
+  unsigned char *KQ = sm + PREP_KQ, *KB = sm + PREP_KB, *TZ = sm + PREP_TZ;
   float *Af = reinterpret_cast<float *>(sm + PREP_AF);
+  float *Xs = reinterpret_cast<float *>(sm + PREP_KB);  // [64][64], after G
+  float *Ys = reinterpret_cast<float *>(sm + PREP_YS);
   float *sgam = reinterpret_cast<float *>(sm + PREP_GAM);
+  float *stf = reinterpret_cast<float *>(sm + PREP_TF);
   float *sbeta = reinterpret_cast<float *>(sm + PREP_BETA);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
+  uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
+  uint64_t *bar_g = bar_tma + 1, *bar_w = bar_tma + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PREP_TSLOT);
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_g, 1);
+    mbar_init(bar_w, 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < 8192 / 16; e += PREP_THREADS)  // rows 64..127 of [T'; 0]
+    reinterpret_cast<uint4 *>(TZ + 8192)[e] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_tma, 32768);
+    tma_load_3d(KQ, &map_k, 0, h, t0, bar_tma);
+    tma_load_3d(KQ + 16384, &map_k, 64, h, t0, bar_tma);
+    tma_load_3d(KQ + 8192, &map_q, 0, h, t0, bar_tma);
+    tma_load_3d(KQ + 16384 + 8192, &map_q, 64, h, t0, bar_tma);
+  }
+  // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
+  float gcol[CH];  // KDA: column `tid` of the chunk's gate
+  if constexpr (KDA) {
+#pragma unroll
+    for (int r = 0; r < CH; ++r)
+      gcol[r] = r < len ? g[((long long)(t0 + r) * H + h) * DK + tid] : 0.f;
+  }
   if (tid < CH) {
     const long long row = (long long)(t0 + tid) * H + h;
     sbeta[tid] = tid < len ? beta[row] : 0.f;
-    if constexpr (!KDA) sgam[tid] = tid < len ? g[row] : 0.f;
+    if constexpr (!KDA) {
+      // inclusive cumulative gate: shuffle scan in each warp, then warp 1
+      // adds warp 0's total
+      float x = tid < len ? g[row] : 0.f;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      sgam[tid] = x;
+    }
   }
-  if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
+  if (tid == 0 && !mbar_wait(bar_tma, 0, err, 1)) abort_flag = 1;
   __syncthreads();
   if constexpr (!KDA) {
-    if (tid == 0) {  // inclusive cumulative gate of the chunk
-      float acc = 0.f;
-      for (int r = 0; r < CH; ++r) {
-        acc += sgam[r];
-        sgam[r] = acc;
-      }
+    if (tid >= 32 && tid < CH) sgam[tid] += sgam[31];
+  }
+  if (abort_flag) return;
+  if (len < CH) {  // padding rows of K and Q are zero
+    const int nz = (CH - len) * 8;
+    for (int e = tid; e < nz * 2; e += PREP_THREADS) {
+      const int a = e / nz, rem = e % nz;
+      const int r = len + rem / 8, cj = rem % 8;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(KQ + a * 16384 + r * 128 + cj * 16) = z;
+      *reinterpret_cast<uint4 *>(KQ + a * 16384 + (CH + r) * 128 + cj * 16) = z;
     }
   }
-  // Operand tiles: thread i fills column i of every row.
-  {
+  __syncthreads();
+  if constexpr (KDA) {
+    // Per-row decays inside the operands, relative to the chunk start:
+    // K^ = e^g K and Q^ = e^g Q (A of G; K^ is also B of W), e^-g K (B of G),
+    // and for the scan Q^, K~ = e^(gC - g) K and e^gC.
     const int i = tid;
     const uint32_t aoff = (uint32_t)(i >> 6) * 16384u, boff = (uint32_t)(i >> 6) * 8192u;
-    const __nv_bfloat16 zero = __float2bfloat16(0.f);
-    if constexpr (KDA) {
-      // decays are split around the middle row so that each factor stays
-      // within exp(+-half the chunk's cumulative decay)
-      float gref = 0.f;
-      for (int r = 0; r < CH / 2; ++r)
-        if (r < len) gref += g[((long long)(t0 + r) * H + h) * DK + i];
-      float gam = 0.f;
-      for (int r = 0; r < CH; ++r) {
-        const long long row = (long long)(t0 + r) * H + h;
-        __nv_bfloat16 kq = zero, qq = zero, kb = zero;
-        if (r < len) {
-          gam += g[row * DK + i];
-          const float e1 = expf(gam - gref), e2 = expf(gref - gam);
-          const float kv = __bfloat162float(k[row * DK + i]);
-          const float qv = __bfloat162float(q[row * DK + i]);
-          kq = __float2bfloat16(kv * e1);
-          qq = __float2bfloat16(qv * e1);
-          kb = __float2bfloat16(kv * e2);
-        }
-        *reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63)) = kq;
-        *reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(CH + r, i & 63)) = qq;
-        *reinterpret_cast<__nv_bfloat16 *>(KB + boff + sw128_offset(r, i & 63)) = kb;
-      }
-    } else {
-      for (int r = 0; r < CH; ++r) {
-        const long long row = (long long)(t0 + r) * H + h;
-        const __nv_bfloat16 kv = r < len ? k[row * DK + i] : zero;
-        const __nv_bfloat16 qv = r < len ? q[row * DK + i] : zero;
-        *reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63)) = kv;
-        *reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(CH + r, i & 63)) = qv;
-      }
+    float gC = 0.f;
+#pragma unroll
+    for (int r = 0; r < CH; ++r) gC += gcol[r];
+    __nv_bfloat16 *qh = w.Qh + tile * CH * DK + i;
+    __nv_bfloat16 *kt = w.Kt + tile * CH * DK + i;
+    float gam = 0.f;
+#pragma unroll
+    for (int r = 0; r < CH; ++r) {
+      gam += gcol[r];
+      const float e1 = __expf(gam), e2 = __expf(-gam), e3 = __expf(gC - gam);
+      __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63));
+      __nv_bfloat16 *pq =
+          reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(CH + r, i & 63));
+      const float kv = __bfloat162float(*pk), qv = __bfloat162float(*pq);
+      const __nv_bfloat16 qhv = __float2bfloat16(qv * e1);
+      *pk = __float2bfloat16(kv * e1);
+      *pq = qhv;
+      *reinterpret_cast<__nv_bfloat16 *>(KB + boff + sw128_offset(r, i & 63)) =
+          __float2bfloat16(kv * e2);
+      qh[r * DK] = qhv;
+      kt[r * DK] = __float2bfloat16(kv * e3);
     }
+    w.gC[tile * DK + i] = expf(gC);
+  }
+  if (tid < CH) {  // column factor of T' = T diag(e^gamma) (GDA) or T (KDA)
+    float f = sbeta[tid];
+    if constexpr (!KDA) f *= __expf(sgam[tid]);
+    stf[tid] = f;
   }
   fence_proxy_async();
   if (warp == 0) {
-    tmem_alloc(tslot, 64);
+    tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -310,25 +397,25 @@ __global__ void __launch_bounds__(PREP_THREADS)
     const uint32_t b0 = KDA ? smem_u32(KB) : smem_u32(KQ);
     const uint32_t bcol = KDA ? 8192u : 16384u;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint64_t ad = sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u);
-      const uint64_t bd = sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u);
-      umma_bf16(tbase, ad, bd, idesc, s > 0);
-    }
-    umma_commit(bar);
-    if (!mbar_wait(bar, 0, err)) abort_flag = 1;
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(tbase + PCOL_G, sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u),
+                sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u), idesc, s > 0);
+    umma_commit(bar_g);
+    if (!mbar_wait(bar_g, 0, err, 2)) abort_flag = 1;
   }
   __syncthreads();
   tc_fence_after();
   if (!abort_flag) {
     // thread = accumulator row: rows 0..63 give A, rows 64..127 give P
     float G[CH];
+    {
+      float v[32];
+      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_G, v);
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      float v[16];
-      tmem_ld16(tbase + ((uint32_t)(32 * warp) << 16) + 16 * cc, v);
+      for (int e = 0; e < 32; ++e) G[e] = v[e];
+      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_G + 32, v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) G[16 * cc + e] = v[e];
+      for (int e = 0; e < 32; ++e) G[32 + e] = v[e];
     }
     if (tid < CH) {
       const int r = tid;
@@ -338,7 +425,7 @@ __global__ void __launch_bounds__(PREP_THREADS)
         float a = 0.f;
         if (j < r) {
           a = br * G[j];
-          if constexpr (!KDA) a *= expf(sgam[r] - sgam[j]);
+          if constexpr (!KDA) a *= __expf(sgam[r] - sgam[j]);
         }
         Af[r * AF_LD + j] = a;
       }
@@ -351,16 +438,16 @@ __global__ void __launch_bounds__(PREP_THREADS)
         if (r < len) {
           if (j <= r) {
             p0 = G[j];
-            if constexpr (!KDA) p0 *= expf(sgam[r] - sgam[j]);
+            if constexpr (!KDA) p0 *= __expf(sgam[r] - sgam[j]);
           }
           if (j + 1 <= r) {
             p1 = G[j + 1];
-            if constexpr (!KDA) p1 *= expf(sgam[r] - sgam[j + 1]);
+            if constexpr (!KDA) p1 *= __expf(sgam[r] - sgam[j + 1]);
           }
         }
         packed[j / 2] = pack_bf16(p0, p1);
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(w.P + (((long long)c * H + h) * CH + r) * CH);
+      uint4 *dst = reinterpret_cast<uint4 *>(w.P + (tile * CH + r) * CH);
 #pragma unroll
       for (int e = 0; e < CH / 8; ++e)
         dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2],
@@ -369,442 +456,479 @@ __global__ void __launch_bounds__(PREP_THREADS)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 64);
-  if (abort_flag) return;
-
-  // T = (I + A)^-1 diag(beta): thread j solves column j by forward
-  // substitution, x_r = [r == j] - sum_{m < r} A[r][m] x_m, in fp32.
-  if (tid < CH) {
-    const int j = tid;
-    float x[CH];
-#pragma unroll
-    for (int r = 0; r < CH; ++r) x[r] = 0.f;
-#pragma unroll
-    for (int r = 0; r < CH; ++r) {
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      const float4 *row = reinterpret_cast<const float4 *>(Af + r * AF_LD);
-#pragma unroll
-      for (int m4 = 0; m4 < (r + 3) / 4; ++m4) {
-        const float4 av = row[m4];
-        a0 = fmaf(av.x, x[4 * m4 + 0], a0);
-        a1 = fmaf(av.y, x[4 * m4 + 1], a1);
-        a2 = fmaf(av.z, x[4 * m4 + 2], a2);
-        a3 = fmaf(av.w, x[4 * m4 + 3], a3);
-      }
-      x[r] = (r == j ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
-    }
-    const float bj = sbeta[j];
-    __nv_bfloat16 *dst = w.T + ((long long)c * H + h) * CH * CH + j;
-#pragma unroll
-    for (int r = 0; r < CH; ++r) dst[r * CH] = __float2bfloat16(x[r] * bj);
+  if (abort_flag) {
+    if (warp == 0) tmem_dealloc(tbase, 256);
+    return;
   }
+
+  // X = (I + A)^-1 in fp32, blocked by 16: diagonal blocks by forward
+  // substitution (one column per thread), then the blocks below the
+  // diagonal level by level, X_ij = -X_ii * (sum_{j <= k < i} A_ik X_kj).
+  if (tid < CH) {
+    const int kb = tid >> 4, cc = tid & 15, o = 16 * kb;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < r; ++m) acc = fmaf(-Af[(o + r) * AF_LD + o + m], x[m], acc);
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Xs[(o + r) * CH + o + cc] = x[r];
+  }
+  __syncthreads();
+  for (int d = 1; d < 4; ++d) {
+    const int nblk = 4 - d;
+    for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int bi = d + b, bj = b;
+      float acc = 0.f;
+      for (int m = 16 * bj; m < 16 * bi; ++m)
+        acc = fmaf(Af[(16 * bi + r) * AF_LD + m], Xs[m * CH + 16 * bj + cc], acc);
+      Ys[b * 256 + r * 16 + cc] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int bi = d + b, bj = b;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        acc = fmaf(Xs[(16 * bi + r) * CH + 16 * bi + m], Ys[b * 256 + m * 16 + cc], acc);
+      Xs[(16 * bi + r) * CH + 16 * bj + cc] = -acc;
+    }
+    __syncthreads();
+  }
+  // T[r][j] = X[r][j] beta_j (to the workspace) and T'[r][j] = T[r][j] e^g_j
+  // (GDA) into [T'; 0]; zero above the diagonal
+  {
+    const int r = tid >> 1, half = tid & 1;
+    float tv[32], tp[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int j = 32 * half + u;
+      const float x = j <= r ? Xs[r * CH + j] : 0.f;
+      tv[u] = x * sbeta[j];
+      tp[u] = x * stf[j];
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(w.T + (tile * CH + r) * CH + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dst[q] = pack8(tv + 8 * q);
+      *reinterpret_cast<uint4 *>(TZ + chunk16(r, 4 * half + q)) = pack8(tp + 8 * q);
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // W (lanes r, columns i) = [T'; 0](r, j) K(i, j), K (or K^) as the MN-major
+  // K rows of KQ: M = 128, N = 128, K = 64
+  if (tid == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      umma_bf16(tbase + PCOL_W, sdesc_kmajor(smem_u32(TZ) + s * 32),
+                sdesc_mnmajor(smem_u32(KQ) + s * 2048, 16384), idesc, s > 0);
+    umma_commit(bar_w);
+    if (!mbar_wait(bar_w, 0, err, 3)) abort_flag = 1;
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (!abort_flag && warp < 2) {  // -W rows r = tid (lanes 0..63)
+    const int r = tid;
+    uint4 *dst = reinterpret_cast<uint4 *>(w.W + (tile * CH + r) * DK);
+#pragma unroll
+    for (int q32 = 0; q32 < 4; ++q32) {
+      float v[32];
+      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_W + 32 * q32, v);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = -v[u];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[4 * q32 + q] = pack8(v + 8 * q);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
-// ---- 3. chunk scan ---------------------------------------------------------------
+// ---- 3. chunk scan (warp-specialised, two-stage pipelined) --------------------
+//
+// One CTA per (sequence, head, half of the value columns): NV = 64 state
+// columns, all chunks of the sequence in order. Roles:
+//   warps 0-3 "scan": own the fp32 state rows (thread i = key row i), turn
+//             X into D and D~, apply the state update, then write outputs;
+//   warps 4-7 "gates": GDA gate scan and decay factors, zero padding rows;
+//   warp 8    lane 0 issues every TMA load and every tcgen05.mma.
+// Inputs of chunk c+1 stream into the other stage while chunk c is worked
+// on; [T; 0] V does not depend on the state and is issued as soon as the
+// stage lands; the state hand-off to the next chunk comes before the output
+// stores.
+constexpr int NV = 64;
+constexpr int SCAN_WARPS = 9;
+constexpr int SCAN_THREADS = SCAN_WARPS * 32;
+// stage (80 KB): K (GDA) or K~ (KDA) [64 r][128 i] | [-W; Q or Q^] [128][128 i] |
+//                V [64 j][64 v] | T [64 r][64 j] | zeros [64][64] | P [64 r][64 j]
+constexpr int ST_K = 0, ST_WQ = 16384, ST_V = 49152, ST_T = 57344, ST_Z = 65536,
+              ST_P = 73728, ST_BYTES = 81920;
+constexpr int ST_TX = 16384 + 32768 + 8192 + 8192 + 8192;  // bytes TMA brings per stage
+constexpr int SC_S = 2 * ST_BYTES;       // S0 bf16 [128 i][64 v] (B of X, MN-major)
+constexpr int SC_D = SC_S + 16384;       // D [64 r][64 v]
+constexpr int SC_DT = SC_D + 8192;       // D~ [64 r][64 v] (GDA)
+constexpr int SC_GATES = SC_DT + 8192;   // 4 sets x (e^g [64], e^(gC-g) [64], e^gC [128]) f32
+constexpr int GATE_SET = 256 * 4;
+constexpr int SC_GSCR = SC_GATES + 4 * GATE_SET;  // 64 f32 gate scan scratch
+constexpr int SC_BARS = SC_GSCR + 256;            // 8 mbarriers
+constexpr int SC_RFLAGS = SC_BARS + 8 * 8;        // 2 x 2 role flags
+constexpr int SC_TSLOT = SC_RFLAGS + 16;
+constexpr int SCAN_SMEM = SC_TSLOT + 8 + 1024;    // + alignment slack
+// TMEM columns (512 allocated): X and O double-buffered, state update
+constexpr uint32_t COL_X0 = 0, COL_S = 128, COL_O0 = 192;
 
-constexpr int SCAN_THREADS = 256;
-// Shared-memory tiles (offsets from a 1024-aligned base). Every tile is made
-// of 128-byte swizzled rows; "rows x cols" below, cols split into 64-wide
-// atom columns stored one after the other.
-constexpr int SC_S = 0;          // S0 bf16 [128 i][128 v]   (B of X, MN-major)
-constexpr int SC_KQ = 32768;     // [K; Q] bf16 [128][128 i] (TMA; K is A of the S update)
-constexpr int SC_V = 65536;      // V bf16 [64 j][128 v]     (TMA; B of X, MN-major)
-constexpr int SC_TZP = 81920;    // T [64 r][64 j] | zeros [64][64] | P [64 r][64 j]
-constexpr int SC_KH = 106496;    // K^ = e^gamma . K [64 j][128 i] (A of W^T, MN-major)
-constexpr int SC_WQ = 122880;    // [-W; Q^] bf16 [128][128 i] (A of X, K-major)
-constexpr int SC_D = 155648;     // D bf16 [64 r][128 v]     (B of the O update)
-constexpr int SC_DT = 172032;    // D~ = e^(gC-gamma) . D    (B of the S update, GDA)
-constexpr int SC_KT = 188416;    // K~ = e^(gC-gamma) . K    (A of the S update, KDA)
-constexpr int SC_SMALL = 204800; // gate scalars, barriers, TMEM address
-constexpr int SC_GAM = SC_SMALL;              // 64 f32: gamma_r (GDA)
-constexpr int SC_EG = SC_GAM + 256;           // 64 f32: exp(gamma_r) (GDA)
-constexpr int SC_EDC = SC_EG + 256;           // 64 f32: exp(gamma_C - gamma_r) (GDA)
-constexpr int SC_GC = SC_EDC + 256;           // 128 f32: exp(gamma_C,i)
-constexpr int SC_BAR = SC_GC + 512;           // 2 mbarriers
-constexpr int SC_TSLOT = SC_BAR + 16;
-constexpr int SCAN_SMEM = SC_TSLOT + 16 + 1024;  // + alignment slack
-constexpr int SC_GAMK = SC_D;    // KDA gamma f32 [64][128] aliases D and D~ (dead then)
-constexpr uint32_t COL_W = 0, COL_X = 64, COL_S = 192;  // TMEM columns (512 allocated)
+// Barrier over the 128 threads of one role (ids 1 and 2). The non-aligned
+// form counts threads, so lanes that reach it at different times are fine;
+// __syncwarp first reconverges the warp after a single-lane wait.
+__device__ __forceinline__ void named_bar(int id) {
+  __syncwarp();
+  asm volatile("barrier.sync %0, 128;" ::"r"(id) : "memory");
+}
 
-struct ScanMaps {
-  CUtensorMap q, k, v, T, P;
+// Bounded wait that also gives up early once another role has aborted. On
+// a timeout the error word records the site (bits 8..15) and chunk (16..).
+__device__ __forceinline__ bool wait_ab(uint64_t *bar, uint32_t parity,
+                                        volatile int *abort_flag, int *err, int site,
+                                        int jc) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return !*abort_flag;
+    if ((i & 1023u) == 1023u && *abort_flag) return false;
+  }
+  set_error(err, kDevTimeout | (site << 8) | ((jc & 0x7fff) << 16));
+  *abort_flag = 1;
+  return false;
+}
+
+// One role's wait: its first thread polls, then the role's barrier publishes
+// the outcome through a flag slot that alternates per call, so every thread
+// of the role takes the same branch even if another role aborts meanwhile.
+struct RoleSync {
+  int id;            // named barrier id
+  int *flags;        // 2 ints in shared memory
+  int calls;         // waits made so far (same in every thread of the role)
+  __device__ bool wait(bool elected, uint64_t *bar, uint32_t parity,
+                       volatile int *abort_flag, int *err, int site, int jc) {
+    int *slot = flags + (calls & 1);
+    ++calls;
+    if (elected) *slot = wait_ab(bar, parity, abort_flag, err, site, jc) ? 0 : 1;
+    named_bar(id);
+    return *reinterpret_cast<volatile int *>(slot) == 0;
+  }
 };
 
-__device__ __forceinline__ uint32_t chunk16(int row, int cj) {
-  return (uint32_t)(row * 128 + ((cj ^ (row & 7)) << 4));
-}
-
-// One CTA per (sequence, head): all chunks of the sequence in order.
 template <bool KDA>
 __global__ void __launch_bounds__(SCAN_THREADS, 1)
-    chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q,
-                      const __grid_constant__ CUtensorMap map_k,
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_v,
                       const __grid_constant__ CUtensorMap map_T,
-                      const __grid_constant__ CUtensorMap map_P, const float *__restrict__ g,
+                      const __grid_constant__ CUtensorMap map_P,
+                      const __grid_constant__ CUtensorMap map_W, const float *__restrict__ g,
                       const float *const *state_in, float *__restrict__ out, int H,
                       float scale, WsPtrs w, int *err) {
   constexpr int DK = 128, DV = 128;
-  const int s = w.order[blockIdx.x / H];
-  const int h = blockIdx.x % H;
+  const int vs = blockIdx.x & 1;  // value-column half
+  const int h = (blockIdx.x >> 1) % H;
+  const int s = w.order[(blockIdx.x >> 1) / H];
   const int nch = w.seq_nch[s];
   if (nch == 0) return;
   const int chunk0 = w.seq_chunk0[s];
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
-  float *sgam = reinterpret_cast<float *>(sm + SC_GAM);
-  float *seg = reinterpret_cast<float *>(sm + SC_EG);
-  float *sedc = reinterpret_cast<float *>(sm + SC_EDC);
-  float *sgc = reinterpret_cast<float *>(sm + SC_GC);
-  float *sgamk = reinterpret_cast<float *>(sm + SC_GAMK);
-  uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + SC_BAR);
-  uint64_t *bar_mma = bar_tma + 1;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BARS);
+  // full[st]: stage st landed; E1[st]: its gates and padding are ready (one
+  // barrier per stage, so the gates role may run a chunk ahead); E4: S0 in
+  // shared memory; E5: X done; E6: D and D~ in shared memory; E7: S and O done.
+  uint64_t *full = bars, *bE1 = bars + 2;  // [2] each
+  uint64_t *bE4 = bars + 4, *bE5 = bars + 5, *bE6 = bars + 6, *bE7 = bars + 7;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SC_TSLOT);
-  __shared__ int abort_flag;
+  __shared__ int abort_flag_s;
+  volatile int *abort_flag = &abort_flag_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, hv = warp >> 2;
-  const int row = 32 * qd + lane;  // TMEM lane this thread reads
-  const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
-
   if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    abort_flag_s = 0;
+    for (int b = 0; b < 8; ++b) mbar_init(&bars[b], 1);
     fence_mbar_init();
-    prefetch_tmap(&map_q);
-    prefetch_tmap(&map_k);
-    prefetch_tmap(&map_v);
-    prefetch_tmap(&map_T);
-    prefetch_tmap(&map_P);
   }
-  // zero tile between T and P (rows 64..127 of the [T; 0] operand and rows
-  // 0..63 of the [0; P] operand)
-  for (int e = tid; e < 8192 / 16; e += SCAN_THREADS)
-    reinterpret_cast<uint4 *>(sm + SC_TZP + 8192)[e] = make_uint4(0, 0, 0, 0);
-
-  // fp32 master state: this thread owns S[row][64 hv .. 64 hv + 63]
-  float Sm[64];
-  {
-    const float *src = state_in[s];
-    if (src) {
-      const float4 *p4 =
-          reinterpret_cast<const float4 *>(src + ((long long)h * DK + row) * DV + 64 * hv);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float4 v4 = p4[e];
-        Sm[4 * e] = v4.x; Sm[4 * e + 1] = v4.y; Sm[4 * e + 2] = v4.z; Sm[4 * e + 3] = v4.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) Sm[e] = 0.f;
-    }
-    unsigned char *st = sm + SC_S + hv * 16384;
-#pragma unroll
-    for (int cj = 0; cj < 8; ++cj) {
-      uint4 u;
-      u.x = pack_bf16(Sm[8 * cj], Sm[8 * cj + 1]);
-      u.y = pack_bf16(Sm[8 * cj + 2], Sm[8 * cj + 3]);
-      u.z = pack_bf16(Sm[8 * cj + 4], Sm[8 * cj + 5]);
-      u.w = pack_bf16(Sm[8 * cj + 6], Sm[8 * cj + 7]);
-      *reinterpret_cast<uint4 *>(st + chunk16(row, cj)) = u;
-    }
+  for (int e = tid; e < 8192 / 16; e += SCAN_THREADS) {  // zero tiles of both stages
+    reinterpret_cast<uint4 *>(sm + ST_Z)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4 *>(sm + ST_BYTES + ST_Z)[e] = make_uint4(0, 0, 0, 0);
   }
-  fence_proxy_async();
-  if (warp == 0) {
+  if (warp == 8) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  uint32_t mma_phase = 0;
 
-  // single waiter, then a block barrier that publishes the outcome
-  auto wait_mma = [&]() {
-    if (tid == 0 && !mbar_wait(bar_mma, mma_phase, err)) abort_flag = 1;
-    mma_phase ^= 1;
-    __syncthreads();
-    tc_fence_after();
-  };
-
-  for (int jc = 0; jc < nch && !abort_flag; ++jc) {
-    const int gc = chunk0 + jc;
-    const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
-    // B0: TMA loads of K, Q, V, T, P
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_tma, 65536);
-      tma_load_3d(sm + SC_KQ, &map_k, 0, h, t0, bar_tma);
-      tma_load_3d(sm + SC_KQ + 16384, &map_k, 64, h, t0, bar_tma);
-      tma_load_3d(sm + SC_KQ + 8192, &map_q, 0, h, t0, bar_tma);
-      tma_load_3d(sm + SC_KQ + 16384 + 8192, &map_q, 64, h, t0, bar_tma);
-      tma_load_3d(sm + SC_V, &map_v, 0, h, t0, bar_tma);
-      tma_load_3d(sm + SC_V + 8192, &map_v, 64, h, t0, bar_tma);
-      const int trow = (gc * H + h) * CH;
-      tma_load_2d(sm + SC_TZP, &map_T, 0, trow, bar_tma);
-      tma_load_2d(sm + SC_TZP + 16384, &map_P, 0, trow, bar_tma);
-    }
-    // cumulative gates of the chunk (padding rows have g = 0)
-    if constexpr (KDA) {
-      if (tid < DK) {
-        const int i = tid;
-        float gam = 0.f;
-        for (int r = 0; r < CH; ++r) {
-          if (r < len) gam += g[((long long)(t0 + r) * H + h) * DK + i];
-          sgamk[r * DK + i] = gam;
+  if (warp == 8) {
+    // ------------------------------------------------------------ control
+    if (lane == 0) {
+      prefetch_tmap(&map_k);
+      prefetch_tmap(&map_q);
+      prefetch_tmap(&map_v);
+      prefetch_tmap(&map_T);
+      prefetch_tmap(&map_P);
+      prefetch_tmap(&map_W);
+      auto load_stage = [&](int jc) {
+        unsigned char *base = sm + (jc & 1) * ST_BYTES;
+        const int gc = chunk0 + jc;
+        const int t0 = w.chunk_tok[gc];
+        const int trow = (gc * H + h) * CH;
+        uint64_t *fb = &full[jc & 1];
+        mbar_arrive_expect_tx(fb, ST_TX + (KDA ? 512 : 0));
+        if constexpr (KDA) {  // K~ and Q^ tiles from the workspace
+          tma_load_2d(base + ST_K, &map_k, 0, trow, fb);
+          tma_load_2d(base + ST_K + 8192, &map_k, 64, trow, fb);
+          tma_load_2d(base + ST_WQ + 8192, &map_q, 0, trow, fb);
+          tma_load_2d(base + ST_WQ + 16384 + 8192, &map_q, 64, trow, fb);
+          bulk_g2s(sm + SC_GATES + (jc & 3) * GATE_SET + 512,
+                   w.gC + ((long long)gc * H + h) * DK, DK * 4, fb);
+        } else {  // raw K and Q rows of the packed token tensors
+          tma_load_3d(base + ST_K, &map_k, 0, h, t0, fb);
+          tma_load_3d(base + ST_K + 8192, &map_k, 64, h, t0, fb);
+          tma_load_3d(base + ST_WQ + 8192, &map_q, 0, h, t0, fb);
+          tma_load_3d(base + ST_WQ + 16384 + 8192, &map_q, 64, h, t0, fb);
         }
-        sgc[i] = expf(gam);
-      }
-    } else {
-      if (tid < CH) sgam[tid] = tid < len ? g[(long long)(t0 + tid) * H + h] : 0.f;
-    }
-    __syncthreads();
-    if constexpr (!KDA) {
-      if (tid == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < CH; ++r) {
-          acc += sgam[r];
-          sgam[r] = acc;
-        }
-        sgc[0] = expf(acc);
-      }
-      __syncthreads();
-      if (tid < CH) {
-        seg[tid] = expf(sgam[tid]);
-        sedc[tid] = expf(sgam[CH - 1] - sgam[tid]);
-      }
-    }
-    if (tid == 0 && !mbar_wait(bar_tma, jc & 1, err)) abort_flag = 1;
-    __syncthreads();
-    if (abort_flag) break;
-
-    // B1: padding rows of K, Q, V are zero
-    if (len < CH) {
-      const int nz = (CH - len) * 8;  // 16-byte chunks per 64-wide atom row set
-      for (int e = tid; e < nz * 2; e += SCAN_THREADS) {
-        const int a = e / nz, rem = e % nz;
-        const int r = len + rem / 8, cj = rem % 8;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm + SC_KQ + a * 16384 + r * 128 + cj * 16) = z;
-        *reinterpret_cast<uint4 *>(sm + SC_KQ + a * 16384 + (CH + r) * 128 + cj * 16) = z;
-        *reinterpret_cast<uint4 *>(sm + SC_V + a * 8192 + r * 128 + cj * 16) = z;
-      }
-      __syncthreads();
-    }
-    // B2: K^ = e^gamma . K, Q^ = e^gamma . Q (into WQ rows 64..127), K~ (KDA)
-    for (int e = tid; e < CH * 16; e += SCAN_THREADS) {
-      const int r = e >> 4, cc = e & 15, a = cc >> 3, cj = cc & 7;
-      const uint32_t o = chunk16(r, cj);
-      const uint4 ku = *reinterpret_cast<const uint4 *>(sm + SC_KQ + a * 16384 + o);
-      const uint4 qu = *reinterpret_cast<const uint4 *>(sm + SC_KQ + a * 16384 + CH * 128 + o);
-      const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(&ku);
-      const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&qu);
-      float kh[8], qh[8], kt[8];
+        tma_load_2d(base + ST_WQ, &map_W, 0, trow, fb);
+        tma_load_2d(base + ST_WQ + 16384, &map_W, 64, trow, fb);
+        tma_load_3d(base + ST_V, &map_v, NV * vs, h, t0, fb);
+        tma_load_2d(base + ST_T, &map_T, 0, trow, fb);
+        tma_load_2d(base + ST_P, &map_P, 0, trow, fb);
+      };
+      constexpr uint32_t id_x = idesc_bf16_f32(128, 64, false, true);
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 64, true, true);
+      load_stage(0);
+      if (nch > 1) load_stage(1);
+      for (int jc = 0; jc < nch; ++jc) {
+        const uint32_t ph = jc & 1;
+        unsigned char *base = sm + (jc & 1) * ST_BYTES;
+        const uint32_t colx = COL_X0 + 64u * (jc & 1);
+        const uint32_t colo = COL_O0 + 64u * (jc & 1);
+        if (!wait_ab(&bE1[jc & 1], (jc >> 1) & 1, abort_flag, err, 11, jc)) break;
+        tc_fence_after();
+        // X = [T; 0] V  (the state-free part)
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const float kv = __bfloat162float(kb[x]), qv = __bfloat162float(qb[x]);
-        if constexpr (KDA) {
-          const int i = a * 64 + cj * 8 + x;
-          const float gm = sgamk[r * DK + i];
-          const float eg = expf(gm);
-          kh[x] = kv * eg;
-          qh[x] = qv * eg;
-          kt[x] = kv * expf(sgamk[(CH - 1) * DK + i] - gm);
-        } else {
-          kh[x] = kv * seg[r];
-          qh[x] = qv * seg[r];
-          kt[x] = 0.f;
+        for (int k4 = 0; k4 < 4; ++k4)
+          umma_bf16(tbase + colx, sdesc_kmajor(smem_u32(base + ST_T) + k4 * 32),
+                    sdesc_mnmajor(smem_u32(base + ST_V) + k4 * 2048, 8192), id_x, k4 > 0);
+        // the stage chunk jc-1 used is free once its last products finished
+        if (jc >= 1 && jc + 1 < nch) {
+          if (!wait_ab(bE7, (jc - 1) & 1, abort_flag, err, 12, jc)) break;
+          load_stage(jc + 1);
+        }
+        if (!wait_ab(bE4, ph, abort_flag, err, 14, jc)) break;
+        tc_fence_after();
+        // X += [-W; Q^] S0
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8)
+          umma_bf16(tbase + colx,
+                    sdesc_kmajor(smem_u32(base + ST_WQ) + (k8 >> 2) * 16384 + (k8 & 3) * 32),
+                    sdesc_mnmajor(smem_u32(sm + SC_S) + k8 * 2048, 8192), id_x, true);
+        umma_commit(bE5);
+        if (!wait_ab(bE6, ph, abort_flag, err, 15, jc)) break;
+        tc_fence_after();
+        // S_acc = K~^T D~ ; O_acc = [0; P] D
+        const uint32_t bs = KDA ? smem_u32(sm + SC_D) : smem_u32(sm + SC_DT);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          umma_bf16(tbase + COL_S, sdesc_mnmajor(smem_u32(base + ST_K) + k4 * 2048, 8192),
+                    sdesc_mnmajor(bs + k4 * 2048, 8192), id_s, k4 > 0);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          umma_bf16(tbase + colo, sdesc_kmajor(smem_u32(base + ST_Z) + k4 * 32),
+                    sdesc_mnmajor(smem_u32(sm + SC_D) + k4 * 2048, 8192), id_x, k4 > 0);
+        umma_commit(bE7);
+      }
+      if (!*abort_flag) wait_ab(bE7, (nch - 1) & 1, abort_flag, err, 16, nch - 1);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ gates
+    const int pt = tid - 128;
+    float *gscr = reinterpret_cast<float *>(sm + SC_GSCR);
+    RoleSync rs{2, reinterpret_cast<int *>(sm + SC_RFLAGS) + 2, 0};
+    for (int jc = 0; jc < nch; ++jc) {
+      const int st = jc & 1;
+      unsigned char *base = sm + st * ST_BYTES;
+      float *gset = reinterpret_cast<float *>(sm + SC_GATES + (jc & 3) * GATE_SET);
+      const int gc = chunk0 + jc;
+      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      float gv = 0.f;
+      if constexpr (!KDA) {
+        if (pt < len) gv = g[(long long)(t0 + pt) * H + h];
+      }
+      if (!rs.wait(pt == 0, &full[st], (jc >> 1) & 1, abort_flag, err, 21, jc)) break;
+      if (len < CH) {  // padding rows: V always, raw K and Q for GDA
+        const int nz = (CH - len) * 8;
+        for (int e = pt; e < nz * 2; e += 128) {
+          const int a = e / nz, rem = e % nz;
+          const int r = len + rem / 8, cj = rem % 8;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          if constexpr (!KDA) {
+            *reinterpret_cast<uint4 *>(base + ST_K + a * 8192 + r * 128 + cj * 16) = z;
+            *reinterpret_cast<uint4 *>(base + ST_WQ + a * 16384 + (CH + r) * 128 + cj * 16) =
+                z;
+          }
+          if (a == 0) *reinterpret_cast<uint4 *>(base + ST_V + r * 128 + cj * 16) = z;
         }
       }
-      uint4 o1, o2;
-      o1.x = pack_bf16(kh[0], kh[1]); o1.y = pack_bf16(kh[2], kh[3]);
-      o1.z = pack_bf16(kh[4], kh[5]); o1.w = pack_bf16(kh[6], kh[7]);
-      o2.x = pack_bf16(qh[0], qh[1]); o2.y = pack_bf16(qh[2], qh[3]);
-      o2.z = pack_bf16(qh[4], qh[5]); o2.w = pack_bf16(qh[6], qh[7]);
-      *reinterpret_cast<uint4 *>(sm + SC_KH + a * 8192 + o) = o1;
-      *reinterpret_cast<uint4 *>(sm + SC_WQ + a * 16384 + CH * 128 + o) = o2;
-      if constexpr (KDA) {
-        uint4 o3;
-        o3.x = pack_bf16(kt[0], kt[1]); o3.y = pack_bf16(kt[2], kt[3]);
-        o3.z = pack_bf16(kt[4], kt[5]); o3.w = pack_bf16(kt[6], kt[7]);
-        *reinterpret_cast<uint4 *>(sm + SC_KT + a * 8192 + o) = o3;
-      }
-    }
-    fence_proxy_async();
-    __syncthreads();
-
-    // B3: W^T = K^^T T^T  (M = i 128, N = r 64, K = j 64)
-    if (tid == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 64, true, false);
+      if constexpr (!KDA) {
+        // inclusive scan of the 64 scalar gates (warps 4 and 5)
+        if (pt < CH) {
+          float x = gv;
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint64_t ad = sdesc_mnmajor(smem_u32(sm + SC_KH) + st * 2048, 8192);
-        const uint64_t bd = sdesc_kmajor(smem_u32(sm + SC_TZP) + st * 32);
-        umma_bf16(tbase + COL_W, ad, bd, idesc, st > 0);
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+          }
+          gscr[pt] = x;
+        }
+        named_bar(2);
+        if (pt >= 32 && pt < CH) gscr[pt] += gscr[31];
+        named_bar(2);
+        if (pt < CH) {
+          const float gm = gscr[pt], gCs = gscr[CH - 1];
+          gset[pt] = expf(gm);             // e^gamma_r       (output scale)
+          gset[64 + pt] = expf(gCs - gm);  // e^(gC - gamma_r) (D~)
+          if (pt == 0) gset[128] = expf(gCs);
+        }
       }
-      umma_commit(bar_mma);
+      fence_proxy_async();
+      named_bar(2);
+      if (pt == 0) mbar_arrive(&bE1[st]);
     }
-    wait_mma();
-    if (abort_flag) break;
-    // B4: -W (rows r) into WQ rows 0..63, column i = row
+  } else {
+    // ------------------------------------------------------------ scan
+    const int i = tid;  // key row / TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    RoleSync rs{1, reinterpret_cast<int *>(sm + SC_RFLAGS), 0};
+    float Sm[NV];
     {
-      float wv[32];
-      float t16[16];
-      tmem_ld16(tbase + lane_off + COL_W + 32 * hv, t16);
+      const float *src = state_in[s];
+      if (src) {
+        const float4 *p4 = reinterpret_cast<const float4 *>(
+            src + ((long long)h * DK + i) * DV + NV * vs);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) wv[x] = t16[x];
-      tmem_ld16(tbase + lane_off + COL_W + 32 * hv + 16, t16);
+        for (int e = 0; e < NV / 4; ++e) {
+          const float4 v4 = p4[e];
+          Sm[4 * e] = v4.x; Sm[4 * e + 1] = v4.y; Sm[4 * e + 2] = v4.z; Sm[4 * e + 3] = v4.w;
+        }
+      } else {
 #pragma unroll
-      for (int x = 0; x < 16; ++x) wv[16 + x] = t16[x];
-      const int i = row;
-      unsigned char *base = sm + SC_WQ + (i >> 6) * 16384;
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const int r = 32 * hv + x;
-        *reinterpret_cast<__nv_bfloat16 *>(base + sw128_offset(r, i & 63)) =
-            __float2bfloat16(-wv[x]);
+        for (int e = 0; e < NV; ++e) Sm[e] = 0.f;
       }
+#pragma unroll
+      for (int cj = 0; cj < 8; ++cj)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
     }
     fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // B5: X = [-W; Q^] S0 + [T; 0] V  (M = 128, N = 128, K = 128 + 64)
-    if (tid == 0) {
+    named_bar(1);
+    if (i == 0) mbar_arrive(bE4);
+    for (int jc = 0; jc < nch; ++jc) {
+      const uint32_t ph = jc & 1;
+      const uint32_t colx = COL_X0 + 64u * (jc & 1);
+      const uint32_t colo = COL_O0 + 64u * (jc & 1);
+      const float *gset = reinterpret_cast<const float *>(sm + SC_GATES + (jc & 3) * GATE_SET);
+      const int gc = chunk0 + jc;
+      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      // D rows (TMEM lanes 0..63) -> D and D~ tiles
+      if (!rs.wait(i == 0, bE5, ph, abort_flag, err, 31, jc)) break;
       tc_fence_after();
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, true);
+      if (warp < 2) {
+        float dec = 1.f;
+        if constexpr (!KDA) dec = gset[64 + i];
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint64_t ad =
-            sdesc_kmajor(smem_u32(sm + SC_WQ) + (st >> 2) * 16384 + (st & 3) * 32);
-        const uint64_t bd = sdesc_mnmajor(smem_u32(sm + SC_S) + st * 2048, 16384);
-        umma_bf16(tbase + COL_X, ad, bd, idesc_s, st > 0);
-      }
+        for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+          float dv[32];
+          tmem_ld32(tbase + lane_off + colx + 32 * hh, dv);
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint64_t ad = sdesc_kmajor(smem_u32(sm + SC_TZP) + st * 32);
-        const uint64_t bd = sdesc_mnmajor(smem_u32(sm + SC_V) + st * 2048, 8192);
-        umma_bf16(tbase + COL_X, ad, bd, idesc_s, true);
-      }
-      umma_commit(bar_mma);
-    }
-    wait_mma();
-    if (abort_flag) break;
-    // B6: D rows (TMEM lanes 0..63) -> D and D~ tiles
-    if (qd < 2) {
-      const int r = row;
-      float dv[64];
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4 *>(sm + SC_D + chunk16(i, 4 * hh + q)) = pack8(dv + 8 * q);
+          if constexpr (!KDA) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float t16[16];
-        tmem_ld16(tbase + lane_off + COL_X + 64 * hv + 16 * cc, t16);
+            for (int e = 0; e < 32; ++e) dv[e] *= dec;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dv[16 * cc + x] = t16[x];
-      }
-      unsigned char *dbase = sm + SC_D + hv * 8192;
-      unsigned char *tbase_d = sm + SC_DT + hv * 8192;
-      const float dec = KDA ? 1.f : sedc[r];
-#pragma unroll
-      for (int cj = 0; cj < 8; ++cj) {
-        uint4 u;
-        u.x = pack_bf16(dv[8 * cj], dv[8 * cj + 1]);
-        u.y = pack_bf16(dv[8 * cj + 2], dv[8 * cj + 3]);
-        u.z = pack_bf16(dv[8 * cj + 4], dv[8 * cj + 5]);
-        u.w = pack_bf16(dv[8 * cj + 6], dv[8 * cj + 7]);
-        *reinterpret_cast<uint4 *>(dbase + chunk16(r, cj)) = u;
-        if constexpr (!KDA) {
-          uint4 t;
-          t.x = pack_bf16(dv[8 * cj] * dec, dv[8 * cj + 1] * dec);
-          t.y = pack_bf16(dv[8 * cj + 2] * dec, dv[8 * cj + 3] * dec);
-          t.z = pack_bf16(dv[8 * cj + 4] * dec, dv[8 * cj + 5] * dec);
-          t.w = pack_bf16(dv[8 * cj + 6] * dec, dv[8 * cj + 7] * dec);
-          *reinterpret_cast<uint4 *>(tbase_d + chunk16(r, cj)) = t;
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4 *>(sm + SC_DT + chunk16(i, 4 * hh + q)) =
+                  pack8(dv + 8 * q);
+          }
         }
       }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // B7: S_acc = K~^T D~ (M = i, N = v, K = r); X += [0; P] D (K = r')
-    if (tid == 0) {
+      fence_proxy_async();
+      tc_fence_before();
+      named_bar(1);
+      if (i == 0) mbar_arrive(bE6);
+      // state update, handed to the next chunk before the outputs are written
+      if (!rs.wait(i == 0, bE7, ph, abort_flag, err, 32, jc)) break;
       tc_fence_after();
-      constexpr uint32_t idesc_u = idesc_bf16_f32(128, 128, true, true);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
-      const uint32_t a_s = KDA ? smem_u32(sm + SC_KT) : smem_u32(sm + SC_KQ);
-      const uint32_t a_lbo = KDA ? 8192u : 16384u;
-      const uint32_t b_s = KDA ? smem_u32(sm + SC_D) : smem_u32(sm + SC_DT);
+      {
+        const float gcs = KDA ? gset[128 + i] : gset[128];
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint64_t ad = sdesc_mnmajor(a_s + st * 2048, a_lbo);
-        const uint64_t bd = sdesc_mnmajor(b_s + st * 2048, 8192);
-        umma_bf16(tbase + COL_S, ad, bd, idesc_u, st > 0);
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tbase + lane_off + COL_S + 32 * hh, v);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) Sm[32 * hh + u] = fmaf(gcs, Sm[32 * hh + u], v[u]);
+        }
+#pragma unroll
+        for (int cj = 0; cj < 8; ++cj)
+          *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
       }
+      fence_proxy_async();
+      tc_fence_before();
+      named_bar(1);
+      if (i == 0 && jc + 1 < nch) mbar_arrive(bE4);
+      if (warp >= 2) {  // outputs: rows 64..127 of X and of the output accumulator
+        const int r = i - CH;
+        const float qf = KDA ? 1.f : gset[r];
+        float *orow = out + ((long long)(t0 + r) * H + h) * DV + NV * vs;
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint64_t ad = sdesc_kmajor(smem_u32(sm + SC_TZP) + 8192 + st * 32);
-        const uint64_t bd = sdesc_mnmajor(smem_u32(sm + SC_D) + st * 2048, 8192);
-        umma_bf16(tbase + COL_X, ad, bd, idesc_o, true);
-      }
-      umma_commit(bar_mma);
-    }
-    wait_mma();
-    if (abort_flag) break;
-    // B8: S = e^gC . S + S_acc (fp32 master, bf16 operand copy); O rows out
-    {
-      const float gcs = KDA ? sgc[row] : sgc[0];
-      unsigned char *st = sm + SC_S + hv * 16384;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float t16[16];
-        tmem_ld16(tbase + lane_off + COL_S + 64 * hv + 16 * cc, t16);
-#pragma unroll
-        for (int x = 0; x < 16; ++x) Sm[16 * cc + x] = fmaf(gcs, Sm[16 * cc + x], t16[x]);
-      }
-#pragma unroll
-      for (int cj = 0; cj < 8; ++cj) {
-        uint4 u;
-        u.x = pack_bf16(Sm[8 * cj], Sm[8 * cj + 1]);
-        u.y = pack_bf16(Sm[8 * cj + 2], Sm[8 * cj + 3]);
-        u.z = pack_bf16(Sm[8 * cj + 4], Sm[8 * cj + 5]);
-        u.w = pack_bf16(Sm[8 * cj + 6], Sm[8 * cj + 7]);
-        *reinterpret_cast<uint4 *>(st + chunk16(row, cj)) = u;
-      }
-      if (qd >= 2) {
-        const int r = row - CH;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float t16[16];
-          tmem_ld16(tbase + lane_off + COL_X + 64 * hv + 16 * cc, t16);
+        for (int hh = 0; hh < 2; ++hh) {
+          float xv[32], ov[32];
+          tmem_ld32(tbase + lane_off + colx + 32 * hh, xv);
+          tmem_ld32(tbase + lane_off + colo + 32 * hh, ov);
           if (r < len) {
-            float4 *dst = reinterpret_cast<float4 *>(
-                out + ((long long)(t0 + r) * H + h) * DV + 64 * hv + 16 * cc);
+            float4 *dst = reinterpret_cast<float4 *>(orow + 32 * hh);
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
-              dst[x] = make_float4(scale * t16[4 * x], scale * t16[4 * x + 1],
-                                   scale * t16[4 * x + 2], scale * t16[4 * x + 3]);
+            for (int u = 0; u < 8; ++u)
+              dst[u] = make_float4(scale * fmaf(qf, xv[4 * u], ov[4 * u]),
+                                   scale * fmaf(qf, xv[4 * u + 1], ov[4 * u + 1]),
+                                   scale * fmaf(qf, xv[4 * u + 2], ov[4 * u + 2]),
+                                   scale * fmaf(qf, xv[4 * u + 3], ov[4 * u + 3]));
           }
         }
       }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-  }
-
-  if (!abort_flag) {  // state after the chunked part, read by the tail
-    float4 *dst = reinterpret_cast<float4 *>(
-        w.states + (((long long)s * H + h) * DK + row) * DV + 64 * hv);
+    if (!*abort_flag) {  // state after the chunked part, read by the tail
+      float4 *dst = reinterpret_cast<float4 *>(w.states +
+                                               (((long long)s * H + h) * DK + i) * DV + NV * vs);
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
+      for (int e = 0; e < NV / 4; ++e)
+        dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 512);
+  if (warp == 8) {
+    __syncwarp();
+    tmem_dealloc(tbase, 512);
+  }
 }
 
 }  // namespace
@@ -846,10 +970,11 @@ bool map_tokens(CUtensorMap *m, const void *base, int ntok, int H, int D) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 [rows][64]; 64 x 64 boxes, 128-byte swizzle
-bool map_rows64(CUtensorMap *m, const void *base, long long rows) {
-  const cuuint64_t dims[2] = {64, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {128};
+// bf16 [rows][width] workspace tiles (width 64 or 128); 64 x 64 boxes,
+// 128-byte swizzle
+bool map_rows(CUtensorMap *m, const void *base, long long rows, int width) {
+  const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
   const cuuint32_t box[2] = {64, 64}, es[2] = {1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -885,8 +1010,14 @@ cudaError_t set_attributes() {
 
 }  // namespace
 
+// The public size query has no gate mode, so it returns the larger (KDA)
+// layout; a GDA call needs less and fits in it.
 size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk, int Dv, int) {
-  return ws_layout(n_seqs, total_tokens, H, Dk, Dv).total;
+  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, true).total;
+}
+
+size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda) {
+  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, kda).total;
 }
 
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
@@ -894,7 +1025,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
   cudaError_t e = set_attributes();
   if (e != cudaSuccess) return e;
-  const WsLayout lay = ws_layout(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv);
+  const WsLayout lay = ws_layout(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda);
   if (a.workspace_bytes < lay.total) return cudaErrorInvalidValue;
   const WsPtrs w = ws_ptrs(a.workspace, lay);
   const long long state_elems = (long long)a.H * a.Dk * a.Dv;
@@ -905,31 +1036,31 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (a.total_tokens > 0) {
-    const long long prep_grid = lay.max_chunks * a.H;
-    const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const auto *k = static_cast<const __nv_bfloat16 *>(a.k);
-    if (a.kda)
-      chunk_prep_kernel<true><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          q, k, a.g, a.beta, a.H, w, a.err);
-    else
-      chunk_prep_kernel<false><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          q, k, a.g, a.beta, a.H, w, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-    CUtensorMap mq, mk, mv, mT, mP;
+    CUtensorMap mq, mk, mv, mT, mP, mW, mQh, mKt;
     const long long trows = lay.max_chunks * a.H * CH;
     if (!map_tokens(&mq, a.q, a.total_tokens, a.H, a.Dk) ||
         !map_tokens(&mk, a.k, a.total_tokens, a.H, a.Dk) ||
-        !map_tokens(&mv, a.v, a.total_tokens, a.H, a.Dv) || !map_rows64(&mT, w.T, trows) ||
-        !map_rows64(&mP, w.P, trows))
+        !map_tokens(&mv, a.v, a.total_tokens, a.H, a.Dv) ||
+        !map_rows(&mT, w.T, trows, CH) || !map_rows(&mP, w.P, trows, CH) ||
+        !map_rows(&mW, w.W, trows, a.Dk))
       return cudaErrorInvalidValue;
-    const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H);
+    if (a.kda && (!map_rows(&mQh, w.Qh, trows, a.Dk) || !map_rows(&mKt, w.Kt, trows, a.Dk)))
+      return cudaErrorInvalidValue;
+    const long long prep_grid = lay.max_chunks * a.H;
+    if (a.kda)
+      chunk_prep_kernel<true><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
+          mq, mk, a.g, a.beta, a.H, w, a.err);
+    else
+      chunk_prep_kernel<false><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
+          mq, mk, a.g, a.beta, a.H, w, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
     if (a.kda)
       chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mq, mk, mv, mT, mP, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mKt, mQh, mv, mT, mP, mW, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
     else
       chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mq, mk, mv, mT, mP, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mk, mq, mv, mT, mP, mW, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
@@ -953,11 +1084,11 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
 // latency-critical loops where a cudaMalloc (which may synchronise the whole
 // device) is not acceptable. For them the chunked path can run from a fixed
 // scratch area compiled into the library. It is a plain device array, so
-// every GPU that loads this library's chunked kernels keeps it (64 MiB)
+// every GPU that loads this library's chunked kernels keeps it (256 MiB)
 // until the process exits.
 namespace gdn {
 
-constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+constexpr size_t kStaticScratchBytes = size_t(256) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
@@ -971,7 +1102,7 @@ size_t static_scratch_bytes() { return kStaticScratchBytes; }
 // (and launches nothing) when *need exceeds the static area. The first call
 // on a device looks up the area's device address with that device current.
 cudaError_t launch_chunked_static(ChunkedArgs a, cudaStream_t stream, size_t *need) {
-  *need = chunked_workspace_size(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.n_slots);
+  *need = chunked_workspace_need(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda);
   if (*need > kStaticScratchBytes) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -70,12 +70,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete, polling at most kMaxPolls
-// times. Returns false (and sets the error word) if the wait ran out.
+// times. Returns false (and sets the error word, with `site` in bits 8..15)
+// if the wait ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          int *err) {
+                                          int *err, int site = 0) {
   for (uint32_t i = 0; i < kMaxPolls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-  set_error(err, kDevTimeout);
+  set_error(err, kDevTimeout | (site << 8));
   return false;
 }
 

@@ -43,6 +43,8 @@ struct ChunkedArgs {
 
 size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk,
                               int Dv, int n_slots);
+// Bytes one call of the given gate mode needs (at most the size above).
+size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda);
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream);
 
 // The chunked path on the library's fixed scratch area (no workspace

@@ -71,6 +71,62 @@ struct RecCfg {
   static_assert(RAW_QK % 16 == 0 && RAW_V % 16 == 0, "bulk copy alignment");
 };
 
+// One token on a lane's slice of the state (rows rg + ROWG*m, 4 columns):
+// decay, read u = (aS)^T k, correct d = beta (v - u), write S += k d^T,
+// query o = S^T q. Returns the lane's 4 outputs summed over the row groups
+// (before the output scale). The order of the arithmetic is fixed by the
+// configuration alone, never by T, K or the grid.
+template <class C>
+__device__ __forceinline__ float4 token_update(float4 (&st)[C::RPT], const float *kr,
+                                               const float *qr, const float *ar, float a_h,
+                                               float beta, float4 vv, int rg) {
+  constexpr int ROWG = C::ROWG, CG = C::CG, RPT = C::RPT;
+  float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < RPT; ++m) {
+    const int i = rg + ROWG * m;
+    float a = a_h;
+    if constexpr (C::KDA) a = ar[i];
+    const float kv = kr[i];
+    st[m].x *= a; st[m].y *= a; st[m].z *= a; st[m].w *= a;
+    u0 = fmaf(st[m].x, kv, u0);
+    u1 = fmaf(st[m].y, kv, u1);
+    u2 = fmaf(st[m].z, kv, u2);
+    u3 = fmaf(st[m].w, kv, u3);
+  }
+#pragma unroll
+  for (int off = CG; off < 32; off <<= 1) {
+    u0 += __shfl_xor_sync(0xffffffffu, u0, off);
+    u1 += __shfl_xor_sync(0xffffffffu, u1, off);
+    u2 += __shfl_xor_sync(0xffffffffu, u2, off);
+    u3 += __shfl_xor_sync(0xffffffffu, u3, off);
+  }
+  const float d0 = beta * (vv.x - u0), d1 = beta * (vv.y - u1);
+  const float d2 = beta * (vv.z - u2), d3 = beta * (vv.w - u3);
+  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < RPT; ++m) {
+    const int i = rg + ROWG * m;
+    const float kv = kr[i], qv = qr[i];
+    st[m].x = fmaf(kv, d0, st[m].x);
+    st[m].y = fmaf(kv, d1, st[m].y);
+    st[m].z = fmaf(kv, d2, st[m].z);
+    st[m].w = fmaf(kv, d3, st[m].w);
+    o0 = fmaf(st[m].x, qv, o0);
+    o1 = fmaf(st[m].y, qv, o1);
+    o2 = fmaf(st[m].z, qv, o2);
+    o3 = fmaf(st[m].w, qv, o3);
+  }
+#pragma unroll
+  for (int off = CG; off < 32; off <<= 1) {
+    o0 += __shfl_xor_sync(0xffffffffu, o0, off);
+    o1 += __shfl_xor_sync(0xffffffffu, o1, off);
+    o2 += __shfl_xor_sync(0xffffffffu, o2, off);
+    o3 += __shfl_xor_sync(0xffffffffu, o3, off);
+  }
+  return make_float4(o0, o1, o2, o3);
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NT)
     recurrent_kernel(const RecParams p) {
@@ -172,7 +228,7 @@ __global__ void __launch_bounds__(C::NT)
     const uint32_t parity = (tile >> 1) & 1;
     const int n = min(TT, T_s - tile * TT);
     if (warp == 0 && tile + 1 < ntiles) issue(tile + 1, b ^ 1);
-    if (tid == 0 && !mbar_wait(&bar[b], parity, p.err)) abort_flag = 1;
+    if (tid == 0 && !mbar_wait(&bar[b], parity, p.err, 3)) abort_flag = 1;
     // gate and beta scalars of this tile (GDA gate is one value per token)
     if (tid < n) {
       const long long row = (t0 + tile * TT + tid) * p.H + h;
@@ -210,54 +266,11 @@ __global__ void __launch_bounds__(C::NT)
       float a_h = 1.f;
       if constexpr (!C::KDA) a_h = fa[r];
 
-      // decay + read: u = (a S)^T k over this lane's rows
-      float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
-#pragma unroll
-      for (int m = 0; m < RPT; ++m) {
-        const int i = rg + ROWG * m;
-        float a = a_h;
-        if constexpr (C::KDA) a = fa[r * DK + i];
-        const float kv = kr[i];
-        st[m].x *= a; st[m].y *= a; st[m].z *= a; st[m].w *= a;
-        u0 = fmaf(st[m].x, kv, u0);
-        u1 = fmaf(st[m].y, kv, u1);
-        u2 = fmaf(st[m].z, kv, u2);
-        u3 = fmaf(st[m].w, kv, u3);
-      }
-#pragma unroll
-      for (int off = CG; off < 32; off <<= 1) {
-        u0 += __shfl_xor_sync(0xffffffffu, u0, off);
-        u1 += __shfl_xor_sync(0xffffffffu, u1, off);
-        u2 += __shfl_xor_sync(0xffffffffu, u2, off);
-        u3 += __shfl_xor_sync(0xffffffffu, u3, off);
-      }
-      // correct
       const float4 vv =
           *reinterpret_cast<const float4 *>(fv + r * CCOLS + (wcol - col_base));
-      const float d0 = beta * (vv.x - u0), d1 = beta * (vv.y - u1);
-      const float d2 = beta * (vv.z - u2), d3 = beta * (vv.w - u3);
-      // write + query
-      float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-      for (int m = 0; m < RPT; ++m) {
-        const int i = rg + ROWG * m;
-        const float kv = kr[i], qv = qr[i];
-        st[m].x = fmaf(kv, d0, st[m].x);
-        st[m].y = fmaf(kv, d1, st[m].y);
-        st[m].z = fmaf(kv, d2, st[m].z);
-        st[m].w = fmaf(kv, d3, st[m].w);
-        o0 = fmaf(st[m].x, qv, o0);
-        o1 = fmaf(st[m].y, qv, o1);
-        o2 = fmaf(st[m].z, qv, o2);
-        o3 = fmaf(st[m].w, qv, o3);
-      }
-#pragma unroll
-      for (int off = CG; off < 32; off <<= 1) {
-        o0 += __shfl_xor_sync(0xffffffffu, o0, off);
-        o1 += __shfl_xor_sync(0xffffffffu, o1, off);
-        o2 += __shfl_xor_sync(0xffffffffu, o2, off);
-        o3 += __shfl_xor_sync(0xffffffffu, o3, off);
-      }
+      const float4 o = token_update<C>(st, kr, qr, C::KDA ? fa + r * DK : nullptr, a_h, beta,
+                                       vv, rg);
+      const float o0 = o.x, o1 = o.y, o2 = o.z, o3 = o.w;
       if (rg == 0) {
         float *orow = p.out + ((t0 + t) * p.H + h) * DV + wcol;
         st_f4(orow, make_float4(p.scale * o0, p.scale * o1, p.scale * o2, p.scale * o3));
@@ -289,11 +302,11 @@ struct RecPick<64, 64, KDA, Tin> { using C = RecCfg<64, 64, 4, 2, KDA, Tin>; };
 template <int DK, int DV, bool KDA, typename Tin>
 cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
   using C = typename RecPick<DK, DV, KDA, Tin>::C;
-  const long long grid = (long long)p.n_seqs * p.H * C::CTAS_PER_HEAD;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long n_items = (long long)p.n_seqs * p.H * C::CTAS_PER_HEAD;
+  if (n_items == 0) return cudaSuccess;
+  if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   static_assert(C::SMEM <= 48 * 1024, "fits the default shared-memory window");
-  recurrent_kernel<C><<<(unsigned)grid, C::NT, C::SMEM, stream>>>(p);
+  recurrent_kernel<C><<<(unsigned)n_items, C::NT, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -128,7 +128,8 @@ typedef struct {
   float scale;        /* 0 means 1/sqrt(D_k) */
 } gdn_varlen_shape;
 
-/* Bytes of device workspace gdn_forward_chunked needs for this shape. */
+/* Bytes of device workspace gdn_forward_chunked needs for this shape in either
+ * gate mode (the per-row gate mode needs more; this is its figure). */
 size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots);
 
 /*
@@ -156,12 +157,14 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
  * that must never pay for a device allocation (cudaMalloc can synchronise the
  * whole device). This entry point computes exactly what gdn_forward_chunked
  * computes, with the same arguments minus the workspace; its scratch is a
- * fixed 64 MiB device array inside the library, which every GPU that loads
+ * fixed 256 MiB device array inside the library, which every GPU that loads
  * the chunked kernels holds until the process exits.
- *  - Limit: shapes whose gdn_chunked_workspace_size exceeds
+ *  - Limit: shapes whose workspace for the given mode exceeds
  *    gdn_noalloc_scratch_bytes() are rejected with GDN_ERR_UNSUPPORTED and a
- *    message naming both sizes (e.g. 1 x 4096 tokens x 32 heads needs about
- *    36 MB and fits; 8 x ~4k tokens x 16 heads does not).
+ *    message naming both sizes. The scalar-gate mode needs about 33 KB per
+ *    (chunk of 64 tokens, head), the per-row mode about 65 KB, plus 64 KB of
+ *    fp32 state per (sequence, head): 1 x 4096 tokens x 32 heads needs about
+ *    140 MB per-row and fits; 8 x ~4k tokens x 16 heads does not.
  *  - The first call on a device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
  *  - Every call on a device shares the one array and it keeps the previous
