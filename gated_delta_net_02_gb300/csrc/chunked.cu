@@ -26,8 +26,8 @@
 //     cores (tcgen05, accumulator in TMEM) gives A and P; T comes from a
 //     blocked fp32 inverse; W = [T'; 0] K is a second tcgen05 product (T' =
 //     T diag(e^g) and raw K for GDA; T and K^ = e^g . K for KDA). T, P and -W
-//     go to the workspace as bf16, and for KDA also Q^ = e^g . Q,
-//     K~ = e^(gC - g) . K and e^gC.
+//     go to the workspace as bf16, and for KDA also Q^ = e^g . Q and
+//     K~ = e^(gC - g) . K; the gate factors the scan needs go there in fp32.
 //  3. chunk_scan_kernel (one CTA per sequence, head and half of the value
 //     columns, sequential over the chunks): only the state-dependent chain,
 //     [D; Q^ S0] = [-W; Q^] S0 + [T; 0] V, then S = e^gC . S0 + K~^T D~ and
@@ -53,11 +53,13 @@ constexpr int CH = 64;  // chunk length
 // ---- workspace layout --------------------------------------------------------
 //
 // Per (chunk, head) tiles, bf16 row-major: T and P [64][64], -W [64][128];
-// KDA adds Q^ and K~ [64][128] and e^gC fp32 [128].
+// KDA adds Q^ and K~ [64][128]. Per (chunk, head) gate factors, fp32 [256]:
+// GDA e^gamma_r [0, 64), e^(gamma_C - gamma_r) [64, 128), e^gamma_C [128, 256);
+// KDA e^gamma_C,i [128, 256) (the rest 1).
 
 struct WsLayout {
   size_t hdr, chunk_seq, chunk_tok, chunk_len, seq_chunk0, seq_nch, tail_start,
-      tail_len, order, state_ptrs, states, T, P, W, Qh, Kt, gC, total;
+      tail_len, order, state_ptrs, states, T, P, W, Qh, Kt, gs, total;
   long long max_chunks;
 };
 
@@ -89,7 +91,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
   w.W = take(2 * tiles * CH * Dk);
   w.Qh = kda ? take(2 * tiles * CH * Dk) : w.W;
   w.Kt = kda ? take(2 * tiles * CH * Dk) : w.W;
-  w.gC = kda ? take(4 * tiles * Dk) : w.W;
+  w.gs = take(4 * tiles * 256);
   w.total = off;
   return w;
 }
@@ -100,7 +102,7 @@ struct WsPtrs {
   const float **state_ptrs;
   float *states;
   __nv_bfloat16 *T, *P, *W, *Qh, *Kt;
-  float *gC;
+  float *gs;
 };
 
 WsPtrs ws_ptrs(void *base, const WsLayout &w) {
@@ -122,7 +124,7 @@ WsPtrs ws_ptrs(void *base, const WsLayout &w) {
   p.W = reinterpret_cast<__nv_bfloat16 *>(b + w.W);
   p.Qh = reinterpret_cast<__nv_bfloat16 *>(b + w.Qh);
   p.Kt = reinterpret_cast<__nv_bfloat16 *>(b + w.Kt);
-  p.gC = reinterpret_cast<float *>(b + w.gC);
+  p.gs = reinterpret_cast<float *>(b + w.gs);
   return p;
 }
 
@@ -144,12 +146,6 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
   u.z = pack_bf16(x[4], x[5]);
   u.w = pack_bf16(x[6], x[7]);
   return u;
-}
-
-__device__ __forceinline__ void unpack8(uint4 u, float *x) {
-  const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&u);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) x[k] = __bfloat162float(b[k]);
 }
 
 // ---- 1. work list ---------------------------------------------------------------
@@ -373,7 +369,17 @@ __global__ void __launch_bounds__(PREP_THREADS)
       qh[r * DK] = qhv;
       kt[r * DK] = __float2bfloat16(kv * e3);
     }
-    w.gC[tile * DK + i] = expf(gC);
+    w.gs[tile * 256 + 128 + i] = expf(gC);
+    w.gs[tile * 256 + i] = 1.f;
+  }
+  if constexpr (!KDA) {  // gate factors of the scan
+    const float gCs = sgam[CH - 1];
+    float *gs = w.gs + tile * 256;
+    if (tid < CH) {
+      gs[tid] = expf(sgam[tid]);
+      gs[CH + tid] = expf(gCs - sgam[tid]);
+    }
+    gs[128 + tid] = expf(gCs);
   }
   if (tid < CH) {  // column factor of T' = T diag(e^gamma) (GDA) or T (KDA)
     float f = sbeta[tid];
@@ -560,36 +566,38 @@ __global__ void __launch_bounds__(PREP_THREADS)
 // columns, all chunks of the sequence in order. Roles:
 //   warps 0-3 "scan": own the fp32 state rows (thread i = key row i), turn
 //             X into D and D~, apply the state update, then write outputs;
-//   warps 4-7 "gates": GDA gate scan and decay factors, zero padding rows;
-//   warp 8    lane 0 issues every TMA load and every tcgen05.mma.
-// Inputs of chunk c+1 stream into the other stage while chunk c is worked
-// on; [T; 0] V does not depend on the state and is issued as soon as the
-// stage lands; the state hand-off to the next chunk comes before the output
-// stores.
+//   warp 4    "producer": TMA loads of each chunk's tiles into a two-stage
+//             ring (and zero padding rows of a partial last chunk);
+//   warp 5    "mma": lane 0 issues every tcgen05.mma.
+// Per chunk the state-dependent chain is: X += [-W; Q] S0 (mma) -> D (scan)
+// -> S_acc = K~^T D~ (mma) -> S = e^gC . S0 + S_acc (scan) -> next chunk.
+// [T; 0] V and [0; P] D sit off that chain, as do the loads of the next
+// chunk and the output stores.
 constexpr int NV = 64;
-constexpr int SCAN_WARPS = 9;
+constexpr int SCAN_WARPS = 6;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32;
-// stage (80 KB): K (GDA) or K~ (KDA) [64 r][128 i] | [-W; Q or Q^] [128][128 i] |
-//                V [64 j][64 v] | T [64 r][64 j] | zeros [64][64] | P [64 r][64 j]
+// stage: K (GDA) or K~ (KDA) [64 r][128 i] | [-W; Q or Q^] [128][128 i] |
+//        V [64 j][64 v] | T [64 r][64 j] | zeros [64][64] | P [64 r][64 j] |
+//        gate factors fp32 [256]
 constexpr int ST_K = 0, ST_WQ = 16384, ST_V = 49152, ST_T = 57344, ST_Z = 65536,
-              ST_P = 73728, ST_BYTES = 81920;
-constexpr int ST_TX = 16384 + 32768 + 8192 + 8192 + 8192;  // bytes TMA brings per stage
+              ST_P = 73728, ST_G = 81920, ST_BYTES = 82944;
+constexpr int ST_TX = 16384 + 32768 + 8192 + 8192 + 8192 + 1024;  // bytes TMA brings
 constexpr int SC_S = 2 * ST_BYTES;       // S0 bf16 [128 i][64 v] (B of X, MN-major)
 constexpr int SC_D = SC_S + 16384;       // D [64 r][64 v]
 constexpr int SC_DT = SC_D + 8192;       // D~ [64 r][64 v] (GDA)
-constexpr int SC_GATES = SC_DT + 8192;   // 4 sets x (e^g [64], e^(gC-g) [64], e^gC [128]) f32
-constexpr int GATE_SET = 256 * 4;
-constexpr int SC_GSCR = SC_GATES + 4 * GATE_SET;  // 64 f32 gate scan scratch
-constexpr int SC_BARS = SC_GSCR + 256;            // 8 mbarriers
-constexpr int SC_RFLAGS = SC_BARS + 8 * 8;        // 2 x 2 role flags
-constexpr int SC_TSLOT = SC_RFLAGS + 16;
-constexpr int SCAN_SMEM = SC_TSLOT + 8 + 1024;    // + alignment slack
+constexpr int SC_BARS = SC_DT + 8192;    // 10 mbarriers
+constexpr int SC_RFLAGS = SC_BARS + 10 * 8;
+constexpr int SC_TSLOT = SC_RFLAGS + 8;
+constexpr int SCAN_SMEM = SC_TSLOT + 8 + 1024;  // + alignment slack
+static_assert(ST_BYTES % 1024 == 0 && SC_S % 1024 == 0, "swizzled tiles are 1024-aligned");
 // TMEM columns (512 allocated): X and O double-buffered, state update
 constexpr uint32_t COL_X0 = 0, COL_S = 128, COL_O0 = 192;
+// polls of the clean-up waits before exit (a healthy one ends at once)
+constexpr uint32_t kDrainPolls = 1u << 22;
 
-// Barrier over the 128 threads of one role (ids 1 and 2). The non-aligned
-// form counts threads, so lanes that reach it at different times are fine;
-// __syncwarp first reconverges the warp after a single-lane wait.
+// Barrier over the 128 scan threads (id 1). The non-aligned form counts
+// threads, so lanes that reach it at different times are fine; __syncwarp
+// first reconverges the warp after a single-lane wait.
 __device__ __forceinline__ void named_bar(int id) {
   __syncwarp();
   asm volatile("barrier.sync %0, 128;" ::"r"(id) : "memory");
@@ -607,6 +615,12 @@ __device__ __forceinline__ bool wait_ab(uint64_t *bar, uint32_t parity,
   set_error(err, kDevTimeout | (site << 8) | ((jc & 0x7fff) << 16));
   *abort_flag = 1;
   return false;
+}
+
+// Wait used only while shutting down: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kDrainPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return;
 }
 
 // One role's wait: its first thread polls, then the role's barrier publishes
@@ -633,7 +647,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_v,
                       const __grid_constant__ CUtensorMap map_T,
                       const __grid_constant__ CUtensorMap map_P,
-                      const __grid_constant__ CUtensorMap map_W, const float *__restrict__ g,
+                      const __grid_constant__ CUtensorMap map_W,
                       const float *const *state_in, float *__restrict__ out, int H,
                       float scale, WsPtrs w, int *err) {
   constexpr int DK = 128, DV = 128;
@@ -646,27 +660,31 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
+  // full[st]: stage st landed; empty[st]: the products reading stage st are
+  // done; E1: padding of a partial last chunk zeroed; E4: S0 in shared
+  // memory; E5: X done; E6: D and D~ in shared memory; E7: S_acc done;
+  // E8: O done; E9: every product issued so far done (shutdown).
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BARS);
-  // full[st]: stage st landed; E1[st]: its gates and padding are ready (one
-  // barrier per stage, so the gates role may run a chunk ahead); E4: S0 in
-  // shared memory; E5: X done; E6: D and D~ in shared memory; E7: S and O done.
-  uint64_t *full = bars, *bE1 = bars + 2;  // [2] each
-  uint64_t *bE4 = bars + 4, *bE5 = bars + 5, *bE6 = bars + 6, *bE7 = bars + 7;
+  uint64_t *full = bars, *empty = bars + 2;  // [2] each
+  uint64_t *bE1 = bars + 4, *bE4 = bars + 5, *bE5 = bars + 6, *bE6 = bars + 7,
+           *bE7 = bars + 8, *bE8 = bars + 9;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SC_TSLOT);
   __shared__ int abort_flag_s;
+  __shared__ uint64_t bE9_s;
   volatile int *abort_flag = &abort_flag_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     abort_flag_s = 0;
-    for (int b = 0; b < 8; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < 10; ++b) mbar_init(&bars[b], 1);
+    mbar_init(&bE9_s, 1);
     fence_mbar_init();
   }
   for (int e = tid; e < 8192 / 16; e += SCAN_THREADS) {  // zero tiles of both stages
     reinterpret_cast<uint4 *>(sm + ST_Z)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4 *>(sm + ST_BYTES + ST_Z)[e] = make_uint4(0, 0, 0, 0);
   }
-  if (warp == 8) {
+  if (warp == 5) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -676,8 +694,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ control
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
     if (lane == 0) {
       prefetch_tmap(&map_k);
       prefetch_tmap(&map_q);
@@ -685,20 +704,26 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       prefetch_tmap(&map_T);
       prefetch_tmap(&map_P);
       prefetch_tmap(&map_W);
-      auto load_stage = [&](int jc) {
-        unsigned char *base = sm + (jc & 1) * ST_BYTES;
-        const int gc = chunk0 + jc;
-        const int t0 = w.chunk_tok[gc];
-        const int trow = (gc * H + h) * CH;
-        uint64_t *fb = &full[jc & 1];
-        mbar_arrive_expect_tx(fb, ST_TX + (KDA ? 512 : 0));
+    }
+    for (int jc = 0; jc < nch; ++jc) {
+      const int st = jc & 1;
+      if (jc >= 2) {  // the products of chunk jc - 2 have released the stage
+        int ok = 1;
+        if (lane == 0) ok = wait_ab(&empty[st], ((jc >> 1) - 1) & 1, abort_flag, err, 41, jc);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      unsigned char *base = sm + st * ST_BYTES;
+      const int gc = chunk0 + jc;
+      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      const int trow = (gc * H + h) * CH;
+      if (lane == 0) {
+        uint64_t *fb = &full[st];
+        mbar_arrive_expect_tx(fb, ST_TX);
         if constexpr (KDA) {  // K~ and Q^ tiles from the workspace
           tma_load_2d(base + ST_K, &map_k, 0, trow, fb);
           tma_load_2d(base + ST_K + 8192, &map_k, 64, trow, fb);
           tma_load_2d(base + ST_WQ + 8192, &map_q, 0, trow, fb);
           tma_load_2d(base + ST_WQ + 16384 + 8192, &map_q, 64, trow, fb);
-          bulk_g2s(sm + SC_GATES + (jc & 3) * GATE_SET + 512,
-                   w.gC + ((long long)gc * H + h) * DK, DK * 4, fb);
         } else {  // raw K and Q rows of the packed token tensors
           tma_load_3d(base + ST_K, &map_k, 0, h, t0, fb);
           tma_load_3d(base + ST_K + 8192, &map_k, 64, h, t0, fb);
@@ -710,29 +735,59 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         tma_load_3d(base + ST_V, &map_v, NV * vs, h, t0, fb);
         tma_load_2d(base + ST_T, &map_T, 0, trow, fb);
         tma_load_2d(base + ST_P, &map_P, 0, trow, fb);
-      };
+        bulk_g2s(base + ST_G, w.gs + ((long long)gc * H + h) * 256, 1024, fb);
+      }
+      ++issued;
+      if (len < CH) {
+        // Only the last chunk can be partial. Its padding rows of V (and of
+        // the raw K and Q for GDA) hold the next tokens: zero them.
+        int ok = 1;
+        if (lane == 0) ok = wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, 42, jc);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        constexpr int per_row = KDA ? 8 : 40;  // 16-byte pieces per padding row
+        for (int e = lane; e < (CH - len) * per_row; e += 32) {
+          const int r = len + e / per_row, c = e % per_row;
+          unsigned char *dst;
+          if (c < 8) {
+            dst = base + ST_V + r * 128 + c * 16;
+          } else if (c < 24) {
+            dst = base + ST_K + ((c - 8) >> 3) * 8192 + r * 128 + ((c - 8) & 7) * 16;
+          } else {
+            dst = base + ST_WQ + ((c - 24) >> 3) * 16384 + (CH + r) * 128 + ((c - 24) & 7) * 16;
+          }
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bE1);
+      }
+    }
+    // copies still in flight (after an abort) land before the CTA exits
+    if (lane == 0)
+      for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
+        drain_wait(&full[j & 1], (j >> 1) & 1);
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ mma
+    if (lane == 0) {
       constexpr uint32_t id_x = idesc_bf16_f32(128, 64, false, true);
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, true, true);
-      load_stage(0);
-      if (nch > 1) load_stage(1);
       for (int jc = 0; jc < nch; ++jc) {
+        const int st = jc & 1;
         const uint32_t ph = jc & 1;
-        unsigned char *base = sm + (jc & 1) * ST_BYTES;
-        const uint32_t colx = COL_X0 + 64u * (jc & 1);
-        const uint32_t colo = COL_O0 + 64u * (jc & 1);
-        if (!wait_ab(&bE1[jc & 1], (jc >> 1) & 1, abort_flag, err, 11, jc)) break;
+        unsigned char *base = sm + st * ST_BYTES;
+        const uint32_t colx = COL_X0 + 64u * ph, colo = COL_O0 + 64u * ph;
+        const bool partial = w.chunk_len[chunk0 + jc] < CH;
+        if (!(partial ? wait_ab(bE1, 0, abort_flag, err, 51, jc)
+                      : wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, 52, jc)))
+          break;
         tc_fence_after();
         // X = [T; 0] V  (the state-free part)
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
           umma_bf16(tbase + colx, sdesc_kmajor(smem_u32(base + ST_T) + k4 * 32),
                     sdesc_mnmajor(smem_u32(base + ST_V) + k4 * 2048, 8192), id_x, k4 > 0);
-        // the stage chunk jc-1 used is free once its last products finished
-        if (jc >= 1 && jc + 1 < nch) {
-          if (!wait_ab(bE7, (jc - 1) & 1, abort_flag, err, 12, jc)) break;
-          load_stage(jc + 1);
-        }
-        if (!wait_ab(bE4, ph, abort_flag, err, 14, jc)) break;
+        if (!wait_ab(bE4, ph, abort_flag, err, 53, jc)) break;
         tc_fence_after();
         // X += [-W; Q^] S0
 #pragma unroll
@@ -741,78 +796,27 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                     sdesc_kmajor(smem_u32(base + ST_WQ) + (k8 >> 2) * 16384 + (k8 & 3) * 32),
                     sdesc_mnmajor(smem_u32(sm + SC_S) + k8 * 2048, 8192), id_x, true);
         umma_commit(bE5);
-        if (!wait_ab(bE6, ph, abort_flag, err, 15, jc)) break;
+        if (!wait_ab(bE6, ph, abort_flag, err, 54, jc)) break;
         tc_fence_after();
-        // S_acc = K~^T D~ ; O_acc = [0; P] D
+        // S_acc = K~^T D~
         const uint32_t bs = KDA ? smem_u32(sm + SC_D) : smem_u32(sm + SC_DT);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
           umma_bf16(tbase + COL_S, sdesc_mnmajor(smem_u32(base + ST_K) + k4 * 2048, 8192),
                     sdesc_mnmajor(bs + k4 * 2048, 8192), id_s, k4 > 0);
+        umma_commit(bE7);
+        // O = [0; P] D
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
           umma_bf16(tbase + colo, sdesc_kmajor(smem_u32(base + ST_Z) + k4 * 32),
                     sdesc_mnmajor(smem_u32(sm + SC_D) + k4 * 2048, 8192), id_x, k4 > 0);
-        umma_commit(bE7);
+        umma_commit(bE8);
+        umma_commit(&empty[st]);
       }
-      if (!*abort_flag) wait_ab(bE7, (nch - 1) & 1, abort_flag, err, 16, nch - 1);
+      umma_commit(&bE9_s);  // tracks every product issued above
+      drain_wait(&bE9_s, 0);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ gates
-    const int pt = tid - 128;
-    float *gscr = reinterpret_cast<float *>(sm + SC_GSCR);
-    RoleSync rs{2, reinterpret_cast<int *>(sm + SC_RFLAGS) + 2, 0};
-    for (int jc = 0; jc < nch; ++jc) {
-      const int st = jc & 1;
-      unsigned char *base = sm + st * ST_BYTES;
-      float *gset = reinterpret_cast<float *>(sm + SC_GATES + (jc & 3) * GATE_SET);
-      const int gc = chunk0 + jc;
-      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
-      float gv = 0.f;
-      if constexpr (!KDA) {
-        if (pt < len) gv = g[(long long)(t0 + pt) * H + h];
-      }
-      if (!rs.wait(pt == 0, &full[st], (jc >> 1) & 1, abort_flag, err, 21, jc)) break;
-      if (len < CH) {  // padding rows: V always, raw K and Q for GDA
-        const int nz = (CH - len) * 8;
-        for (int e = pt; e < nz * 2; e += 128) {
-          const int a = e / nz, rem = e % nz;
-          const int r = len + rem / 8, cj = rem % 8;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          if constexpr (!KDA) {
-            *reinterpret_cast<uint4 *>(base + ST_K + a * 8192 + r * 128 + cj * 16) = z;
-            *reinterpret_cast<uint4 *>(base + ST_WQ + a * 16384 + (CH + r) * 128 + cj * 16) =
-                z;
-          }
-          if (a == 0) *reinterpret_cast<uint4 *>(base + ST_V + r * 128 + cj * 16) = z;
-        }
-      }
-      if constexpr (!KDA) {
-        // inclusive scan of the 64 scalar gates (warps 4 and 5)
-        if (pt < CH) {
-          float x = gv;
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-          }
-          gscr[pt] = x;
-        }
-        named_bar(2);
-        if (pt >= 32 && pt < CH) gscr[pt] += gscr[31];
-        named_bar(2);
-        if (pt < CH) {
-          const float gm = gscr[pt], gCs = gscr[CH - 1];
-          gset[pt] = expf(gm);             // e^gamma_r       (output scale)
-          gset[64 + pt] = expf(gCs - gm);  // e^(gC - gamma_r) (D~)
-          if (pt == 0) gset[128] = expf(gCs);
-        }
-      }
-      fence_proxy_async();
-      named_bar(2);
-      if (pt == 0) mbar_arrive(&bE1[st]);
-    }
   } else {
     // ------------------------------------------------------------ scan
     const int i = tid;  // key row / TMEM lane
@@ -841,18 +845,25 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     named_bar(1);
     if (i == 0) mbar_arrive(bE4);
     for (int jc = 0; jc < nch; ++jc) {
+      const int st = jc & 1;
       const uint32_t ph = jc & 1;
-      const uint32_t colx = COL_X0 + 64u * (jc & 1);
-      const uint32_t colo = COL_O0 + 64u * (jc & 1);
-      const float *gset = reinterpret_cast<const float *>(sm + SC_GATES + (jc & 3) * GATE_SET);
+      const uint32_t colx = COL_X0 + 64u * ph, colo = COL_O0 + 64u * ph;
       const int gc = chunk0 + jc;
       const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
-      // D rows (TMEM lanes 0..63) -> D and D~ tiles
       if (!rs.wait(i == 0, bE5, ph, abort_flag, err, 31, jc)) break;
       tc_fence_after();
+      // gate factors of this chunk: the stage landed before X could finish;
+      // the wait gives each thread its own view of it (never blocks here)
+      drain_wait(&full[st], (jc >> 1) & 1);
+      const float *gs = reinterpret_cast<const float *>(sm + st * ST_BYTES + ST_G);
+      const float gcs = gs[128 + i];
+      float dec = 1.f, qf = 1.f;
+      if constexpr (!KDA) {
+        if (warp < 2) dec = gs[64 + i];
+        else qf = gs[i - CH];
+      }
+      // D rows (TMEM lanes 0..63) -> D and D~ tiles
       if (warp < 2) {
-        float dec = 1.f;
-        if constexpr (!KDA) dec = gset[64 + i];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
           float dv[32];
@@ -877,26 +888,25 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       // state update, handed to the next chunk before the outputs are written
       if (!rs.wait(i == 0, bE7, ph, abort_flag, err, 32, jc)) break;
       tc_fence_after();
-      {
-        const float gcs = KDA ? gset[128 + i] : gset[128];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[32];
-          tmem_ld32(tbase + lane_off + COL_S + 32 * hh, v);
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+        tmem_ld32(tbase + lane_off + COL_S + 32 * hh, v);
 #pragma unroll
-          for (int u = 0; u < 32; ++u) Sm[32 * hh + u] = fmaf(gcs, Sm[32 * hh + u], v[u]);
-        }
-#pragma unroll
-        for (int cj = 0; cj < 8; ++cj)
-          *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
+        for (int u = 0; u < 32; ++u) Sm[32 * hh + u] = fmaf(gcs, Sm[32 * hh + u], v[u]);
       }
+#pragma unroll
+      for (int cj = 0; cj < 8; ++cj)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
       fence_proxy_async();
       tc_fence_before();
       named_bar(1);
       if (i == 0 && jc + 1 < nch) mbar_arrive(bE4);
-      if (warp >= 2) {  // outputs: rows 64..127 of X and of the output accumulator
+      // outputs: rows 64..127 of X (Q S0) and of O (P D)
+      if (!rs.wait(i == 0, bE8, ph, abort_flag, err, 34, jc)) break;
+      tc_fence_after();
+      if (warp >= 2) {
         const int r = i - CH;
-        const float qf = KDA ? 1.f : gset[r];
         float *orow = out + ((long long)(t0 + r) * H + h) * DV + NV * vs;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -914,6 +924,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
           }
         }
       }
+      tc_fence_before();
     }
     if (!*abort_flag) {  // state after the chunked part, read by the tail
       float4 *dst = reinterpret_cast<float4 *>(w.states +
@@ -925,7 +936,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 5) {
     __syncwarp();
     tmem_dealloc(tbase, 512);
   }
@@ -1038,6 +1049,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if (a.total_tokens > 0) {
     CUtensorMap mq, mk, mv, mT, mP, mW, mQh, mKt;
     const long long trows = lay.max_chunks * a.H * CH;
+    if (trows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are int32
     if (!map_tokens(&mq, a.q, a.total_tokens, a.H, a.Dk) ||
         !map_tokens(&mk, a.k, a.total_tokens, a.H, a.Dk) ||
         !map_tokens(&mv, a.v, a.total_tokens, a.H, a.Dv) ||
@@ -1057,10 +1069,10 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
     if (a.kda)
       chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mKt, mQh, mv, mT, mP, mW, a.state_in, a.out, a.H, a.scale, w, a.err);
     else
       chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, a.g, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mk, mq, mv, mT, mP, mW, a.state_in, a.out, a.H, a.scale, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
