@@ -390,6 +390,11 @@ gdn_status gdn_check_device_error(gdn_stream_t stream) {
       return fail(GDN_ERR_DEVICE_ARG, "cu_seqlens is not a valid offset table");
     case gdn::kDevOverlap:
       return fail(GDN_ERR_DEVICE_ARG, "a state_in pointer points into state_slots");
+    case gdn::kDevGateRange:
+      return fail(GDN_ERR_DEVICE_ARG,
+                  "a gate decays (or grows) by more than e^80 inside one 64-token chunk; the "
+                  "chunked path cannot represent that decay, run these sequences through "
+                  "gdn_forward");
     default:
       return fail(GDN_ERR_DEVICE_ARG, "device error word %d", word);
   }

@@ -239,29 +239,41 @@ __global__ void __launch_bounds__(WL_THREADS)
 
 // ---- 2. chunk preparation (all state-independent products) -------------------
 
-constexpr int PREP_THREADS = 128;
-constexpr int AF_LD = 68;  // fp32 row stride of A in shared memory (16-byte rows)
+constexpr int PREP_THREADS = 256;
+constexpr int XS_LD = 68;  // fp32 row stride of X (16-byte rows, conflict-free row reads)
 // Shared memory, offsets from a 1024-aligned base:
-//  KQ [128][128] bf16: K rows 0..63, Q rows 64..127 (TMA; KDA scales them in
-//     place to K^ = e^g . K and Q^ = e^g . Q). A of G; its K rows are B of W.
-//  KB [64][128] bf16: KDA e^-g . K (B of G); afterwards the fp32 inverse X.
-//  AF [64][AF_LD] fp32: A.   TZ [128][64] bf16: [T'; 0], A of W.
-constexpr int PREP_KQ = 0, PREP_KB = 32768, PREP_AF = 49152;
-constexpr int PREP_TZ = PREP_AF + 64 * AF_LD * 4;  // 1024-aligned
-constexpr int PREP_YS = PREP_TZ + 16384;           // [3][16][16] f32 level products
-constexpr int PREP_GAM = PREP_YS + 3072;           // [64] f32 gamma (GDA)
-constexpr int PREP_TF = PREP_GAM + 256;            // [64] f32 column factor of T'
-constexpr int PREP_BETA = PREP_TF + 256;           // [64] f32
-constexpr int PREP_BAR = PREP_BETA + 256;          // 3 mbarriers
+//  KQ [128][128] bf16 in two 64-column halves of 16 KB: K rows 0..63, Q rows
+//     64..127 (TMA; KDA scales them in place to K^ = e^g . K and Q^ = e^g . Q).
+//     A of G; its K rows are also B of W. Once G is done the Q rows hold A
+//     (fp32, rows 0..31 in half 0 and rows 32..63 in half 1, see af_off).
+//  TZ [64][64] bf16: T', rows 0..63 of the A operand of W (rows 64..127 of
+//     that operand read the next 8 KB, whose products are never used).
+//  KB [64][128] bf16: KDA e^-g . K (B of G); afterwards X fp32 [64][XS_LD].
+constexpr int PREP_KQ = 0, PREP_TZ = 32768, PREP_KB = 40960;
+constexpr int PREP_GAM = PREP_KB + 64 * XS_LD * 4;  // [64] f32 gamma (GDA)
+constexpr int PREP_TF = PREP_GAM + 256;             // [64] f32 column factor of T'
+constexpr int PREP_BETA = PREP_TF + 256;            // [64] f32
+constexpr int PREP_HSUM = PREP_BETA + 256;          // [2][128] f32 KDA half-chunk gate sums
+constexpr int PREP_BAR = PREP_HSUM + 1024;          // 3 mbarriers
 constexpr int PREP_TSLOT = PREP_BAR + 24;
-constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;   // + alignment slack
-constexpr uint32_t PCOL_G = 0, PCOL_W = 64;        // TMEM columns (256 allocated)
-static_assert(PREP_TZ % 1024 == 0, "TZ holds swizzled atoms");
+constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;    // + alignment slack
+constexpr uint32_t PCOL_G = 0, PCOL_W = 0;          // TMEM columns (128 allocated; W reuses G's)
+static_assert(PREP_TZ % 1024 == 0 && PREP_KB % 1024 == 0, "swizzled atoms are 1024-aligned");
+static_assert(64 * XS_LD * 4 >= 16384, "X region also holds KB");
+
+// Byte offset of A(r, j) (fp32) inside KQ once G is done: rows 0..31 in the
+// Q rows of half 0, rows 32..63 in those of half 1; 64 floats per row with
+// the column XOR-ed by (r & 15), so that 32 threads writing one column of
+// 32 consecutive rows hit 16 different banks, and the swizzle of a row
+// depends only on r mod 16.
+__device__ __forceinline__ uint32_t af_off(int r, int j) {
+  return (uint32_t)((r >> 5) * 16384 + 8192 + (r & 31) * 256 + ((j ^ (r & 15)) << 2));
+}
 
 // One CTA per (chunk, head). Rows r of the chunk are tokens chunk_tok + r,
 // r < len; the rest are padding (k = q = 0, beta = 0, g = 0).
 template <bool KDA>
-__global__ void __launch_bounds__(PREP_THREADS)
+__global__ void __launch_bounds__(PREP_THREADS, 3)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
                       const float *__restrict__ beta, int H, WsPtrs w, int *err) {
@@ -273,12 +285,11 @@ __global__ void __launch_bounds__(PREP_THREADS)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   unsigned char *KQ = sm + PREP_KQ, *KB = sm + PREP_KB, *TZ = sm + PREP_TZ;
-  float *Af = reinterpret_cast<float *>(sm + PREP_AF);
-  float *Xs = reinterpret_cast<float *>(sm + PREP_KB);  // [64][64], after G
-  float *Ys = reinterpret_cast<float *>(sm + PREP_YS);
+  float *Xs = reinterpret_cast<float *>(sm + PREP_KB);  // [64][XS_LD], after G
   float *sgam = reinterpret_cast<float *>(sm + PREP_GAM);
   float *stf = reinterpret_cast<float *>(sm + PREP_TF);
   float *sbeta = reinterpret_cast<float *>(sm + PREP_BETA);
+  float *hsum = reinterpret_cast<float *>(sm + PREP_HSUM);
   uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
   uint64_t *bar_g = bar_tma + 1, *bar_w = bar_tma + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PREP_TSLOT);
@@ -292,8 +303,6 @@ __global__ void __launch_bounds__(PREP_THREADS)
     mbar_init(bar_w, 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < 8192 / 16; e += PREP_THREADS)  // rows 64..127 of [T'; 0]
-    reinterpret_cast<uint4 *>(TZ + 8192)[e] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_tma, 32768);
@@ -303,11 +312,17 @@ __global__ void __launch_bounds__(PREP_THREADS)
     tma_load_3d(KQ + 16384 + 8192, &map_q, 64, h, t0, bar_tma);
   }
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
-  float gcol[CH];  // KDA: column `tid` of the chunk's gate
+  constexpr int HR = CH / 2;  // KDA: thread (i, half) owns channel i, rows HR*half..
+  float gcol[KDA ? HR : 1];
   if constexpr (KDA) {
+    const int i = tid & 127, r0 = HR * (tid >> 7);
+    float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < CH; ++r)
-      gcol[r] = r < len ? g[((long long)(t0 + r) * H + h) * DK + tid] : 0.f;
+    for (int r = 0; r < HR; ++r) {
+      gcol[r] = r0 + r < len ? g[((long long)(t0 + r0 + r) * H + h) * DK + i] : 0.f;
+      s += gcol[r];
+    }
+    hsum[(tid >> 7) * 128 + i] = s;
   }
   if (tid < CH) {
     const long long row = (long long)(t0 + tid) * H + h;
@@ -345,17 +360,18 @@ __global__ void __launch_bounds__(PREP_THREADS)
     // Per-row decays inside the operands, relative to the chunk start:
     // K^ = e^g K and Q^ = e^g Q (A of G; K^ is also B of W), e^-g K (B of G),
     // and for the scan Q^, K~ = e^(gC - g) K and e^gC.
-    const int i = tid;
+    const int i = tid & 127, half = tid >> 7, r0 = HR * half;
+    const float gC = hsum[i] + hsum[128 + i];
     const uint32_t aoff = (uint32_t)(i >> 6) * 16384u, boff = (uint32_t)(i >> 6) * 8192u;
-    float gC = 0.f;
-#pragma unroll
-    for (int r = 0; r < CH; ++r) gC += gcol[r];
     __nv_bfloat16 *qh = w.Qh + tile * CH * DK + i;
     __nv_bfloat16 *kt = w.Kt + tile * CH * DK + i;
-    float gam = 0.f;
+    float gam = half ? hsum[i] : 0.f;
+    float gabs = fabsf(gC);
 #pragma unroll
-    for (int r = 0; r < CH; ++r) {
-      gam += gcol[r];
+    for (int rr = 0; rr < HR; ++rr) {
+      const int r = r0 + rr;
+      gam += gcol[rr];
+      gabs = fmaxf(gabs, fabsf(gam));
       const float e1 = __expf(gam), e2 = __expf(-gam), e3 = __expf(gC - gam);
       __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63));
       __nv_bfloat16 *pq =
@@ -369,17 +385,23 @@ __global__ void __launch_bounds__(PREP_THREADS)
       qh[r * DK] = qhv;
       kt[r * DK] = __float2bfloat16(kv * e3);
     }
-    w.gs[tile * 256 + 128 + i] = expf(gC);
-    w.gs[tile * 256 + i] = 1.f;
-  }
-  if constexpr (!KDA) {  // gate factors of the scan
+    if (half == 0) {
+      w.gs[tile * 256 + 128 + i] = expf(gC);
+      w.gs[tile * 256 + i] = 1.f;
+    }
+    if (gabs > kMaxChunkLogDecay) set_error(err, kDevGateRange);
+  } else {  // gate factors of the scan
     const float gCs = sgam[CH - 1];
     float *gs = w.gs + tile * 256;
     if (tid < CH) {
       gs[tid] = expf(sgam[tid]);
       gs[CH + tid] = expf(gCs - sgam[tid]);
+      // decays are exact pairwise differences; only growth can overflow
+      if (sgam[tid] > kMaxChunkLogDecay || gCs - sgam[tid] > kMaxChunkLogDecay)
+        set_error(err, kDevGateRange);
+    } else if (tid < CH + 128) {
+      gs[128 + tid - CH] = expf(gCs);
     }
-    gs[128 + tid] = expf(gCs);
   }
   if (tid < CH) {  // column factor of T' = T diag(e^gamma) (GDA) or T (KDA)
     float f = sbeta[tid];
@@ -388,7 +410,7 @@ __global__ void __launch_bounds__(PREP_THREADS)
   }
   fence_proxy_async();
   if (warp == 0) {
-    tmem_alloc(tslot, 256);
+    tmem_alloc(tslot, 128);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -412,50 +434,49 @@ __global__ void __launch_bounds__(PREP_THREADS)
   __syncthreads();
   tc_fence_after();
   if (!abort_flag) {
-    // thread = accumulator row: rows 0..63 give A, rows 64..127 give P
-    float G[CH];
-    {
-      float v[32];
-      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_G, v);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) G[e] = v[e];
-      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_G + 32, v);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) G[32 + e] = v[e];
-    }
-    if (tid < CH) {
-      const int r = tid;
+    // thread = accumulator row (TMEM lane group warp & 3) and 32 columns
+    // (warp >> 2): rows 0..63 give A (into the Q rows, dead once G is done),
+    // rows 64..127 give P
+    const int row = 32 * (warp & 3) + lane, j0 = 32 * (warp >> 2);
+    float G[32];
+    tmem_ld32(tbase + ((uint32_t)(32 * (warp & 3)) << 16) + PCOL_G + j0, G);
+    if (row < CH) {
+      const int r = row;
       const float br = sbeta[r];
+      const float gr = KDA ? 0.f : sgam[r];
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
+      for (int u = 0; u < 32; ++u) {
+        const int j = j0 + u;
         float a = 0.f;
         if (j < r) {
-          a = br * G[j];
-          if constexpr (!KDA) a *= __expf(sgam[r] - sgam[j]);
+          a = br * G[u];
+          if constexpr (!KDA) a *= __expf(gr - sgam[j]);
         }
-        Af[r * AF_LD + j] = a;
+        *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
       }
     } else {
-      const int r = tid - CH;
-      uint32_t packed[CH / 2];
+      const int r = row - CH;
+      const float gr = KDA ? 0.f : sgam[r];
+      uint32_t packed[16];
 #pragma unroll
-      for (int j = 0; j < CH; j += 2) {
+      for (int u = 0; u < 32; u += 2) {
+        const int j = j0 + u;
         float p0 = 0.f, p1 = 0.f;
         if (r < len) {
           if (j <= r) {
-            p0 = G[j];
-            if constexpr (!KDA) p0 *= __expf(sgam[r] - sgam[j]);
+            p0 = G[u];
+            if constexpr (!KDA) p0 *= __expf(gr - sgam[j]);
           }
           if (j + 1 <= r) {
-            p1 = G[j + 1];
-            if constexpr (!KDA) p1 *= __expf(sgam[r] - sgam[j + 1]);
+            p1 = G[u + 1];
+            if constexpr (!KDA) p1 *= __expf(gr - sgam[j + 1]);
           }
         }
-        packed[j / 2] = pack_bf16(p0, p1);
+        packed[u / 2] = pack_bf16(p0, p1);
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(w.P + (tile * CH + r) * CH);
+      uint4 *dst = reinterpret_cast<uint4 *>(w.P + (tile * CH + r) * CH + j0);
 #pragma unroll
-      for (int e = 0; e < CH / 8; ++e)
+      for (int e = 0; e < 4; ++e)
         dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2],
                             packed[4 * e + 3]);
     }
@@ -463,74 +484,87 @@ __global__ void __launch_bounds__(PREP_THREADS)
   tc_fence_before();
   __syncthreads();
   if (abort_flag) {
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 128);
     return;
   }
 
-  // X = (I + A)^-1 in fp32, blocked by 16: diagonal blocks by forward
-  // substitution (one column per thread), then the blocks below the
-  // diagonal level by level, X_ij = -X_ii * (sum_{j <= k < i} A_ik X_kj).
-  if (tid < CH) {
-    const int kb = tid >> 4, cc = tid & 15, o = 16 * kb;
-    float x[16];
+  // X = (I + A)^-1 in fp32, X[r][c] = delta_rc - sum_{k<r} A[r][k] X[k][c],
+  // as a wavefront over 16-row blocks: thread (c, R) owns rows 16R..16R+15
+  // of column c. At step kb the owner of block kb finishes it by forward
+  // substitution; then every later block adds A(R, kb) X(kb, c). A rows are
+  // broadcast loads (all threads of a warp share R), X(kb, c) comes from
+  // shared memory.
+  {
+    const int cc = tid & 63, R = tid >> 6;
+    const uint32_t rowbase = (uint32_t)((R >> 1) * 16384 + 8192 + (R & 1) * 4096);
+    float acc[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = (r == cc) ? 1.f : 0.f;
+    for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    for (int kb = 0; kb < 4; ++kb) {
+      if (R == kb) {  // finish block R, right-looking
 #pragma unroll
-      for (int m = 0; m < r; ++m) acc = fmaf(-Af[(o + r) * AF_LD + o + m], x[m], acc);
-      x[r] = acc;
+        for (int u = 0; u < 16; ++u) {
+          const float xu = (16 * R + u == cc ? 1.f : 0.f) - acc[u];
+          Xs[(16 * R + u) * XS_LD + cc] = xu;
+#pragma unroll
+          for (int u2 = u + 1; u2 < 16; ++u2)
+            acc[u2] = fmaf(*reinterpret_cast<const float *>(KQ + rowbase + u2 * 256 + 64 * R +
+                                                            4 * (u ^ u2)),
+                           xu, acc[u2]);
+        }
+      }
+      __syncthreads();
+      if (R > kb) {  // contribution of the finished block kb
+#pragma unroll 1
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int k0 = 16 * kb + 4 * k4;
+          float x[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) x[b] = Xs[(k0 + b) * XS_LD + cc];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            // row r = 16R+u keeps A(r, k0 + b) at column 16kb + ((4k4 + b) ^ u):
+            // one float4 at 16kb + (4k4 ^ (u & 12)), element b in lane b ^ (u & 3)
+            const float4 a4 = *reinterpret_cast<const float4 *>(
+                KQ + rowbase + u * 256 + 64 * kb + 4 * ((4 * k4) ^ (u & 12)));
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[u] = fmaf(av[b ^ (u & 3)], x[b], acc[u]);
+          }
+        }
+      }
     }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) Xs[(o + r) * CH + o + cc] = x[r];
   }
   __syncthreads();
-  for (int d = 1; d < 4; ++d) {
-    const int nblk = 4 - d;
-    for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int bi = d + b, bj = b;
-      float acc = 0.f;
-      for (int m = 16 * bj; m < 16 * bi; ++m)
-        acc = fmaf(Af[(16 * bi + r) * AF_LD + m], Xs[m * CH + 16 * bj + cc], acc);
-      Ys[b * 256 + r * 16 + cc] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int bi = d + b, bj = b;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        acc = fmaf(Xs[(16 * bi + r) * CH + 16 * bi + m], Ys[b * 256 + m * 16 + cc], acc);
-      Xs[(16 * bi + r) * CH + 16 * bj + cc] = -acc;
-    }
-    __syncthreads();
-  }
-  // T[r][j] = X[r][j] beta_j (to the workspace) and T'[r][j] = T[r][j] e^g_j
-  // (GDA) into [T'; 0]; zero above the diagonal
+  // T[r][j] = X[r][j] beta_j (to the workspace) and T'[r][j] = X[r][j] f_j
+  // into TZ; thread = (row r, 16 columns)
   {
-    const int r = tid >> 1, half = tid & 1;
-    float tv[32], tp[32];
+    const int r = tid & 63, qd = tid >> 6;
+    float tv[16], tp[16];
+    const float4 *xr = reinterpret_cast<const float4 *>(Xs + r * XS_LD + 16 * qd);
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const int j = 32 * half + u;
-      const float x = j <= r ? Xs[r * CH + j] : 0.f;
-      tv[u] = x * sbeta[j];
-      tp[u] = x * stf[j];
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(w.T + (tile * CH + r) * CH + 32 * half);
+    for (int v = 0; v < 4; ++v) {
+      const float4 x4 = xr[v];
+      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      dst[q] = pack8(tv + 8 * q);
-      *reinterpret_cast<uint4 *>(TZ + chunk16(r, 4 * half + q)) = pack8(tp + 8 * q);
+      for (int b = 0; b < 4; ++b) {
+        const int j = 16 * qd + 4 * v + b;
+        tv[4 * v + b] = xv[b] * sbeta[j];
+        tp[4 * v + b] = xv[b] * stf[j];
+      }
     }
+    uint4 *dst = reinterpret_cast<uint4 *>(w.T + (tile * CH + r) * CH + 16 * qd);
+    dst[0] = pack8(tv);
+    dst[1] = pack8(tv + 8);
+    *reinterpret_cast<uint4 *>(TZ + chunk16(r, 2 * qd)) = pack8(tp);
+    *reinterpret_cast<uint4 *>(TZ + chunk16(r, 2 * qd + 1)) = pack8(tp + 8);
   }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // W (lanes r, columns i) = [T'; 0](r, j) K(i, j), K (or K^) as the MN-major
-  // K rows of KQ: M = 128, N = 128, K = 64
+  // W (lanes r, columns i) = T'(r, j) K(i, j), K (or K^) as the MN-major K
+  // rows of KQ: M = 128 (rows 64..127 unused), N = 128, K = 64
   if (tid == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
@@ -542,13 +576,13 @@ __global__ void __launch_bounds__(PREP_THREADS)
   }
   __syncthreads();
   tc_fence_after();
-  if (!abort_flag && warp < 2) {  // -W rows r = tid (lanes 0..63)
-    const int r = tid;
-    uint4 *dst = reinterpret_cast<uint4 *>(w.W + (tile * CH + r) * DK);
+  if (!abort_flag && (warp & 3) < 2) {  // -W: rows r (lanes 0..63), 64 columns per warp
+    const int r = 32 * (warp & 3) + lane, c0 = 64 * (warp >> 2);
+    uint4 *dst = reinterpret_cast<uint4 *>(w.W + (tile * CH + r) * DK + c0);
 #pragma unroll
-    for (int q32 = 0; q32 < 4; ++q32) {
+    for (int q32 = 0; q32 < 2; ++q32) {
       float v[32];
-      tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + PCOL_W + 32 * q32, v);
+      tmem_ld32(tbase + ((uint32_t)(32 * (warp & 3)) << 16) + PCOL_W + c0 + 32 * q32, v);
 #pragma unroll
       for (int u = 0; u < 32; ++u) v[u] = -v[u];
 #pragma unroll
@@ -557,7 +591,7 @@ __global__ void __launch_bounds__(PREP_THREADS)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 256);
+  if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // ---- 3. chunk scan (warp-specialised, two-stage pipelined) --------------------

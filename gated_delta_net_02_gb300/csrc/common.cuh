@@ -15,7 +15,13 @@ enum DevErr : int {
   kDevTimeout = 1,     // a bounded mbarrier wait ran out
   kDevBadSeqlens = 2,  // cu_seqlens is not a valid offset table
   kDevOverlap = 3,     // a state_in pointer points into the slot buffer
+  kDevGateRange = 4,   // a chunk's cumulative log-gate leaves [-80, 80] (chunked path)
 };
+
+// Largest |cumulative log-gate| inside one chunk that the chunked kernels
+// accept: their decay factors e^(+-gamma) are stored in bf16/fp32, whose
+// range ends near e^88.
+constexpr float kMaxChunkLogDecay = 80.f;
 
 // Upper bound on polls of one mbarrier wait. A healthy wait completes in a
 // few thousand polls; ~2^26 polls take well over a second.

@@ -61,7 +61,8 @@ typedef enum {
   GDN_ERR_ROLLBACK_RANGE = 3, /* the requested state was not stored */
   GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
   GDN_ERR_TIMEOUT = 5,        /* a bounded device-side wait ran out */
-  GDN_ERR_DEVICE_ARG = 6      /* the device found a bad argument (cu_seqlens) */
+  GDN_ERR_DEVICE_ARG = 6      /* the device found a bad argument (cu_seqlens, or a
+                                 gate range the chunked path cannot represent) */
 } gdn_status;
 
 typedef enum { GDN_MODE_GDA = 0, GDN_MODE_KDA = 1 } gdn_mode;
@@ -140,6 +141,13 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots);
  * state_slots device fp32 [N][n_slots][H][D_k][D_v]
  * workspace   device buffer of at least gdn_chunked_workspace_size bytes,
  *             256-byte aligned; its contents on entry do not matter.
+ * Gate range: inside each 64-token chunk the cumulative log-gate from the
+ * chunk's first token must stay within [-80, 80] for per-row gates (for
+ * scalar gates only growth above e^80 is limited; any decay is exact). The
+ * chunk form keeps its decay factors e^(+-gamma) in bf16/fp32, whose range
+ * ends near e^88. A chunk outside it leaves its outputs undefined and makes
+ * gdn_check_device_error return GDN_ERR_DEVICE_ARG; gdn_forward (the token
+ * loop) has no such limit.
  */
 gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
                                const int32_t *cu_seqlens, const void *q,

@@ -133,3 +133,30 @@ def test_repeated_calls_reuse_dirty_workspace(gdn):
     out1, sl1 = chunked_forward(gdn, b)
     out2, sl2 = chunked_forward(gdn, b)
     assert torch.equal(out1, out2) and torch.equal(sl1, sl2)
+
+
+def test_kda_strong_decay_inside_range(gdn):
+    # per-row gates ~ -softplus(N(0,1)): a chunk's cumulative log-gate reaches
+    # about -50 to -70 per channel, inside the range the chunk form accepts
+    b = inputs.make_batch(47, [200, 130], 2, 128, 128, mode="kda", n_slots=2,
+                          kda_gate_scale=1.0)
+    gmin = float(torch.cumsum(b.g[:64], dim=0).min())
+    assert -80.0 < gmin < -40.0
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)
+
+
+def test_kda_decay_beyond_range_reported(gdn):
+    # gates 3x stronger leave [-80, 80] inside the first chunk: the device
+    # reports it, and the token-loop entry point still matches the oracle
+    b = inputs.make_batch(48, [200], 2, 128, 128, mode="kda", n_slots=1, kda_gate_scale=3.0)
+    assert float(torch.cumsum(b.g[:64], dim=0).min()) < -80.0
+    chunked_forward(gdn, b, check=False)
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_check_device_error()
+    assert e.value.status == gdn.GDN_ERR_DEVICE_ARG
+    assert "e^80" in str(e.value)
+    out, slots = gpu_forward(b)
+    o_ref, s_ref, _ = oracle_run(b, n_slots=1)
+    assert rel_l2(out.double().cpu().numpy(), o_ref) <= TOL_BF16
+    assert rel_l2(slots[:, -1].double().cpu().numpy(), s_ref) <= TOL_BF16
