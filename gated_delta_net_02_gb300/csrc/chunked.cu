@@ -598,17 +598,20 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
 //
 // One CTA per (sequence, head, half of the value columns): NV = 64 state
 // columns, all chunks of the sequence in order. Roles:
-//   warps 0-3 "scan": own the fp32 state rows (thread i = key row i), turn
-//             X into D and D~, apply the state update, then write outputs;
-//   warp 4    "producer": TMA loads of each chunk's tiles into a two-stage
+//   warps 0-7 "state": thread (key row i = 32 (w & 3) + lane, 32 columns
+//             32 (w >> 2)..) owns that part of the fp32 state; turns X into
+//             D and D~, applies the state update, writes outputs;
+//   warp 8    "producer": TMA loads of each chunk's tiles into a two-stage
 //             ring (and zero padding rows of a partial last chunk);
-//   warp 5    "mma": lane 0 issues every tcgen05.mma.
-// Per chunk the state-dependent chain is: X += [-W; Q] S0 (mma) -> D (scan)
-// -> S_acc = K~^T D~ (mma) -> S = e^gC . S0 + S_acc (scan) -> next chunk.
-// [T; 0] V and [0; P] D sit off that chain, as do the loads of the next
-// chunk and the output stores.
+//   warp 9    "mma": lane 0 issues every tcgen05.mma.
+// Per chunk the state-dependent chain is: X += [-W; Q] S0 (mma) -> D (state)
+// -> S_acc = K~^T D~ (mma) -> S = e^gC . S0 + S_acc (state) -> next chunk.
+// Off that chain: [T; 0] V of the next chunk is issued right behind the
+// state update, [0; P] D right behind the next chunk's [-W; Q] S0, and the
+// outputs of a chunk are stored while the next chunk's state update runs.
 constexpr int NV = 64;
-constexpr int SCAN_WARPS = 6;
+constexpr int STATE_THREADS = 256;
+constexpr int SCAN_WARPS = 10;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32;
 // stage: K (GDA) or K~ (KDA) [64 r][128 i] | [-W; Q or Q^] [128][128 i] |
 //        V [64 j][64 v] | T [64 r][64 j] | zeros [64][64] | P [64 r][64 j] |
@@ -617,24 +620,26 @@ constexpr int ST_K = 0, ST_WQ = 16384, ST_V = 49152, ST_T = 57344, ST_Z = 65536,
               ST_P = 73728, ST_G = 81920, ST_BYTES = 82944;
 constexpr int ST_TX = 16384 + 32768 + 8192 + 8192 + 8192 + 1024;  // bytes TMA brings
 constexpr int SC_S = 2 * ST_BYTES;       // S0 bf16 [128 i][64 v] (B of X, MN-major)
-constexpr int SC_D = SC_S + 16384;       // D [64 r][64 v]
-constexpr int SC_DT = SC_D + 8192;       // D~ [64 r][64 v] (GDA)
-constexpr int SC_BARS = SC_DT + 8192;    // 10 mbarriers
-constexpr int SC_RFLAGS = SC_BARS + 10 * 8;
+constexpr int SC_D = SC_S + 16384;       // D [2][64 r][64 v] (double-buffered)
+constexpr int SC_DT = SC_D + 16384;      // D~ [64 r][64 v] (GDA)
+constexpr int SC_OUT = SC_DT + 8192;    // output staging fp32 [2][64 r][32 v], 128-byte swizzle
+constexpr int SC_BARS = SC_OUT + 16384;  // 11 mbarriers
+constexpr int SC_RFLAGS = SC_BARS + 11 * 8;
 constexpr int SC_TSLOT = SC_RFLAGS + 8;
 constexpr int SCAN_SMEM = SC_TSLOT + 8 + 1024;  // + alignment slack
 static_assert(ST_BYTES % 1024 == 0 && SC_S % 1024 == 0, "swizzled tiles are 1024-aligned");
-// TMEM columns (512 allocated): X and O double-buffered, state update
-constexpr uint32_t COL_X0 = 0, COL_S = 128, COL_O0 = 192;
+// TMEM columns (512 allocated): X triple-buffered (a chunk's Q S0 rows are
+// read after the next chunk's X is issued), state update, O double-buffered
+constexpr uint32_t COL_X0 = 0, COL_S = 192, COL_O0 = 256;
 // polls of the clean-up waits before exit (a healthy one ends at once)
 constexpr uint32_t kDrainPolls = 1u << 22;
 
-// Barrier over the 128 scan threads (id 1). The non-aligned form counts
+// Barrier over the 256 state threads (id 1). The non-aligned form counts
 // threads, so lanes that reach it at different times are fine; __syncwarp
 // first reconverges the warp after a single-lane wait.
 __device__ __forceinline__ void named_bar(int id) {
   __syncwarp();
-  asm volatile("barrier.sync %0, 128;" ::"r"(id) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "n"(STATE_THREADS) : "memory");
 }
 
 // Bounded wait that also gives up early once another role has aborted. On
@@ -682,6 +687,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_T,
                       const __grid_constant__ CUtensorMap map_P,
                       const __grid_constant__ CUtensorMap map_W,
+                      const __grid_constant__ CUtensorMap map_out,
                       const float *const *state_in, float *__restrict__ out, int H,
                       float scale, WsPtrs w, int *err) {
   constexpr int DK = 128, DV = 128;
@@ -697,11 +703,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   // full[st]: stage st landed; empty[st]: the products reading stage st are
   // done; E1: padding of a partial last chunk zeroed; E4: S0 in shared
   // memory; E5: X done; E6: D and D~ in shared memory; E7: S_acc done;
-  // E8: O done; E9: every product issued so far done (shutdown).
+  // E8[j & 1]: O of chunk j done (one per parity: on the last chunk O can
+  // finish before the previous chunk's O is waited for); E9: every product
+  // issued so far done (shutdown).
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SC_BARS);
   uint64_t *full = bars, *empty = bars + 2;  // [2] each
   uint64_t *bE1 = bars + 4, *bE4 = bars + 5, *bE5 = bars + 6, *bE6 = bars + 7,
-           *bE7 = bars + 8, *bE8 = bars + 9;
+           *bE7 = bars + 8, *bE8 = bars + 9;  // bE8 [2]
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SC_TSLOT);
   __shared__ int abort_flag_s;
   __shared__ uint64_t bE9_s;
@@ -710,7 +718,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     abort_flag_s = 0;
-    for (int b = 0; b < 10; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < 11; ++b) mbar_init(&bars[b], 1);
     mbar_init(&bE9_s, 1);
     fence_mbar_init();
   }
@@ -718,7 +726,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     reinterpret_cast<uint4 *>(sm + ST_Z)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4 *>(sm + ST_BYTES + ST_Z)[e] = make_uint4(0, 0, 0, 0);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -728,7 +736,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     int issued = 0;
     if (lane == 0) {
@@ -770,6 +778,25 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         tma_load_2d(base + ST_T, &map_T, 0, trow, fb);
         tma_load_2d(base + ST_P, &map_P, 0, trow, fb);
         bulk_g2s(base + ST_G, w.gs + ((long long)gc * H + h) * 256, 1024, fb);
+        if (jc + 2 < nch) {  // chunk jc + 2 loads into this stage two chunks later: warm L2
+          const int gp = gc + 2, tp = w.chunk_tok[gp], prow = (gp * H + h) * CH;
+          if constexpr (KDA) {
+            tma_prefetch_2d(&map_k, 0, prow);
+            tma_prefetch_2d(&map_k, 64, prow);
+            tma_prefetch_2d(&map_q, 0, prow);
+            tma_prefetch_2d(&map_q, 64, prow);
+          } else {
+            tma_prefetch_3d(&map_k, 0, h, tp);
+            tma_prefetch_3d(&map_k, 64, h, tp);
+            tma_prefetch_3d(&map_q, 0, h, tp);
+            tma_prefetch_3d(&map_q, 64, h, tp);
+          }
+          tma_prefetch_2d(&map_W, 0, prow);
+          tma_prefetch_2d(&map_W, 64, prow);
+          tma_prefetch_3d(&map_v, NV * vs, h, tp);
+          tma_prefetch_2d(&map_T, 0, prow);
+          tma_prefetch_2d(&map_P, 0, prow);
+        }
       }
       ++issued;
       if (len < CH) {
@@ -801,90 +828,185 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
         drain_wait(&full[j & 1], (j >> 1) & 1);
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ mma
     if (lane == 0) {
       constexpr uint32_t id_x = idesc_bf16_f32(128, 64, false, true);
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, true, true);
-      for (int jc = 0; jc < nch; ++jc) {
-        const int st = jc & 1;
-        const uint32_t ph = jc & 1;
-        unsigned char *base = sm + st * ST_BYTES;
-        const uint32_t colx = COL_X0 + 64u * ph, colo = COL_O0 + 64u * ph;
-        const bool partial = w.chunk_len[chunk0 + jc] < CH;
-        if (!(partial ? wait_ab(bE1, 0, abort_flag, err, 51, jc)
-                      : wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, 52, jc)))
-          break;
+      // stage of chunk j usable: landed, or for a partial last chunk padded
+      auto stage_bar = [&](int j, uint32_t *parity) -> uint64_t * {
+        if (w.chunk_len[chunk0 + j] < CH) {
+          *parity = 0;
+          return bE1;
+        }
+        *parity = (j >> 1) & 1;
+        return &full[j & 1];
+      };
+      // X(j) = [T; 0] V (state-free) into X buffer j % 3
+      // shared-memory descriptors of both stages, built once; a K step
+      // advances the start-address field (bytes >> 4) by a plain add
+      const uint32_t sm0 = smem_u32(sm);
+      auto kdesc = [&](uint32_t off) { return sdesc_kmajor(sm0 + off); };
+      auto mdesc = [&](uint32_t off, uint32_t lbo) { return sdesc_mnmajor(sm0 + off, lbo); };
+      const uint64_t dT[2] = {kdesc(ST_T), kdesc(ST_BYTES + ST_T)};
+      const uint64_t dV[2] = {mdesc(ST_V, 8192), mdesc(ST_BYTES + ST_V, 8192)};
+      const uint64_t dWQ[2] = {kdesc(ST_WQ), kdesc(ST_BYTES + ST_WQ)};
+      const uint64_t dK[2] = {mdesc(ST_K, 8192), mdesc(ST_BYTES + ST_K, 8192)};
+      const uint64_t dZ[2] = {kdesc(ST_Z), kdesc(ST_BYTES + ST_Z)};
+      const uint64_t dS = mdesc(SC_S, 8192);
+      const uint64_t dD[2] = {mdesc(SC_D, 8192), mdesc(SC_D + 8192, 8192)};
+      const uint64_t dDT = mdesc(SC_DT, 8192);
+      auto issue_x1 = [&](int j) {
+        const uint32_t colx = COL_X0 + 64u * (uint32_t)(j % 3);
         tc_fence_after();
-        // X = [T; 0] V  (the state-free part)
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
-          umma_bf16(tbase + colx, sdesc_kmajor(smem_u32(base + ST_T) + k4 * 32),
-                    sdesc_mnmajor(smem_u32(base + ST_V) + k4 * 2048, 8192), id_x, k4 > 0);
-        if (!wait_ab(bE4, ph, abort_flag, err, 53, jc)) break;
+          umma_bf16(tbase + colx, dT[j & 1] + 2 * k4, dV[j & 1] + 128 * k4, id_x, k4 > 0);
+      };
+      // X(j) += [-W; Q] S0, once S0 is in shared memory
+      auto issue_x2 = [&](int j) -> bool {
+        const uint32_t colx = COL_X0 + 64u * (uint32_t)(j % 3);
+        if (!wait_ab(bE4, j & 1, abort_flag, err, 53, j)) return false;
         tc_fence_after();
-        // X += [-W; Q^] S0
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8)
-          umma_bf16(tbase + colx,
-                    sdesc_kmajor(smem_u32(base + ST_WQ) + (k8 >> 2) * 16384 + (k8 & 3) * 32),
-                    sdesc_mnmajor(smem_u32(sm + SC_S) + k8 * 2048, 8192), id_x, true);
+          umma_bf16(tbase + colx, dWQ[j & 1] + (k8 >> 2) * 1024 + (k8 & 3) * 2, dS + 128 * k8,
+                    id_x, true);
         umma_commit(bE5);
-        if (!wait_ab(bE6, ph, abort_flag, err, 54, jc)) break;
+        return true;
+      };
+      uint32_t par;
+      uint64_t *sb = stage_bar(0, &par);
+      bool ok = wait_ab(sb, par, abort_flag, err, 52, 0);
+      if (ok) {
+        issue_x1(0);
+        ok = issue_x2(0);
+      }
+      for (int jc = 0; ok && jc < nch; ++jc) {
+        const int st = jc & 1;
+        // wait for D(jc); issue the next chunk's state-free part as soon as
+        // its stage is usable, whichever comes first
+        bool x1_done = jc + 1 >= nch;
+        uint64_t *nb = x1_done ? nullptr : stage_bar(jc + 1, &par);
+        bool d_ready = false;
+        for (uint32_t it = 0; it < kMaxPolls; ++it) {
+          if (!x1_done && mbar_test_wait(nb, par)) {
+            issue_x1(jc + 1);
+            x1_done = true;
+          }
+          if (mbar_test_wait(bE6, jc & 1)) {
+            d_ready = true;
+            break;
+          }
+          if ((it & 1023u) == 1023u && *abort_flag) break;
+        }
+        if (!d_ready || *abort_flag) {
+          if (!d_ready && !*abort_flag) {
+            set_error(err, kDevTimeout | (54 << 8) | ((jc & 0x7fff) << 16));
+            *abort_flag = 1;
+          }
+          break;
+        }
         tc_fence_after();
         // S_acc = K~^T D~
-        const uint32_t bs = KDA ? smem_u32(sm + SC_D) : smem_u32(sm + SC_DT);
+        const uint64_t dB = KDA ? dD[jc & 1] : dDT;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
-          umma_bf16(tbase + COL_S, sdesc_mnmajor(smem_u32(base + ST_K) + k4 * 2048, 8192),
-                    sdesc_mnmajor(bs + k4 * 2048, 8192), id_s, k4 > 0);
+          umma_bf16(tbase + COL_S, dK[st] + 128 * k4, dB + 128 * k4, id_s, k4 > 0);
         umma_commit(bE7);
-        // O = [0; P] D
+        // O = [0; P] D, then the stage is free
+        const uint32_t colo = COL_O0 + 64u * (jc & 1);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
-          umma_bf16(tbase + colo, sdesc_kmajor(smem_u32(base + ST_Z) + k4 * 32),
-                    sdesc_mnmajor(smem_u32(sm + SC_D) + k4 * 2048, 8192), id_x, k4 > 0);
-        umma_commit(bE8);
+          umma_bf16(tbase + colo, dZ[st] + 2 * k4, dD[jc & 1] + 128 * k4, id_x, k4 > 0);
+        umma_commit(&bE8[jc & 1]);
         umma_commit(&empty[st]);
+        if (jc + 1 < nch) {
+          if (!x1_done) {
+            if (!wait_ab(nb, par, abort_flag, err, 52, jc + 1)) break;
+            issue_x1(jc + 1);
+          }
+          if (!issue_x2(jc + 1)) break;
+        }
       }
       umma_commit(&bE9_s);  // tracks every product issued above
       drain_wait(&bE9_s, 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ scan
-    const int i = tid;  // key row / TMEM lane
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    // ------------------------------------------------------------ state
+    const int i = 32 * (warp & 3) + lane;  // key row / TMEM lane
+    const int ch = warp >> 2;              // which 32 of the CTA's 64 columns
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     RoleSync rs{1, reinterpret_cast<int *>(sm + SC_RFLAGS), 0};
-    float Sm[NV];
+    float Sm[32];
     {
       const float *src = state_in[s];
       if (src) {
         const float4 *p4 = reinterpret_cast<const float4 *>(
-            src + ((long long)h * DK + i) * DV + NV * vs);
+            src + ((long long)h * DK + i) * DV + NV * vs + 32 * ch);
 #pragma unroll
-        for (int e = 0; e < NV / 4; ++e) {
+        for (int e = 0; e < 8; ++e) {
           const float4 v4 = p4[e];
           Sm[4 * e] = v4.x; Sm[4 * e + 1] = v4.y; Sm[4 * e + 2] = v4.z; Sm[4 * e + 3] = v4.w;
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < NV; ++e) Sm[e] = 0.f;
+        for (int e = 0; e < 32; ++e) Sm[e] = 0.f;
       }
 #pragma unroll
-      for (int cj = 0; cj < 8; ++cj)
-        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, 4 * ch + q)) = pack8(Sm + 8 * q);
     }
     fence_proxy_async();
     named_bar(1);
-    if (i == 0) mbar_arrive(bE4);
+    if (tid == 0) mbar_arrive(bE4);
+    // outputs of chunk j: rows 64..127 of X (Q S0) and of O (P D). A full
+    // chunk goes through a shared-memory tile and two TMA stores (thread 0
+    // issues them; it waits for the previous pair to have read the tile
+    // before the barrier that precedes the next writes); a partial last
+    // chunk is stored row by row, so no token past its end is touched.
+    auto store_out = [&](int j, float qf) {
+      const int gc = chunk0 + j;
+      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      if ((warp & 3) >= 2) {
+        const int r = i - CH;
+        float xv[32], ov[32];
+        tmem_ld32(tbase + lane_off + COL_X0 + 64u * (uint32_t)(j % 3) + 32 * ch, xv);
+        tmem_ld32(tbase + lane_off + COL_O0 + 64u * (uint32_t)(j & 1) + 32 * ch, ov);
+        float4 o4[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          o4[u] = make_float4(scale * fmaf(qf, xv[4 * u], ov[4 * u]),
+                              scale * fmaf(qf, xv[4 * u + 1], ov[4 * u + 1]),
+                              scale * fmaf(qf, xv[4 * u + 2], ov[4 * u + 2]),
+                              scale * fmaf(qf, xv[4 * u + 3], ov[4 * u + 3]));
+        if (len == CH) {
+          unsigned char *tile = sm + SC_OUT + ch * 8192 + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4 *>(tile + ((u ^ (r & 7)) << 4)) = o4[u];
+        } else if (r < len) {
+          float4 *dst = reinterpret_cast<float4 *>(out + ((long long)(t0 + r) * H + h) * DV +
+                                                   NV * vs + 32 * ch);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) dst[u] = o4[u];
+        }
+      }
+      if (len == CH) {
+        fence_proxy_async();
+        named_bar(1);
+        if (tid == 0) {
+          tma_store_3d(&map_out, NV * vs, h, t0, sm + SC_OUT);
+          tma_store_3d(&map_out, NV * vs + 32, h, t0, sm + SC_OUT + 8192);
+          bulk_commit();
+        }
+      }
+    };
     for (int jc = 0; jc < nch; ++jc) {
       const int st = jc & 1;
-      const uint32_t ph = jc & 1;
-      const uint32_t colx = COL_X0 + 64u * ph, colo = COL_O0 + 64u * ph;
-      const int gc = chunk0 + jc;
-      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
-      if (!rs.wait(i == 0, bE5, ph, abort_flag, err, 31, jc)) break;
+      const uint32_t colx = COL_X0 + 64u * (uint32_t)(jc % 3);
+      if (!rs.wait(tid == 0, bE5, jc & 1, abort_flag, err, 31, jc)) break;
       tc_fence_after();
       // gate factors of this chunk: the stage landed before X could finish;
       // the wait gives each thread its own view of it (never blocks here)
@@ -893,84 +1015,65 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       const float gcs = gs[128 + i];
       float dec = 1.f, qf = 1.f;
       if constexpr (!KDA) {
-        if (warp < 2) dec = gs[64 + i];
+        if (i < CH) dec = gs[64 + i];
         else qf = gs[i - CH];
       }
       // D rows (TMEM lanes 0..63) -> D and D~ tiles
-      if (warp < 2) {
+      if ((warp & 3) < 2) {
+        float dv[32];
+        tmem_ld32(tbase + lane_off + colx + 32 * ch, dv);
+        unsigned char *dbuf = sm + SC_D + (jc & 1) * 8192;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
-          float dv[32];
-          tmem_ld32(tbase + lane_off + colx + 32 * hh, dv);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4 *>(dbuf + chunk16(i, 4 * ch + q)) = pack8(dv + 8 * q);
+        if constexpr (!KDA) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dv[e] *= dec;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4 *>(sm + SC_D + chunk16(i, 4 * hh + q)) = pack8(dv + 8 * q);
-          if constexpr (!KDA) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) dv[e] *= dec;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4 *>(sm + SC_DT + chunk16(i, 4 * hh + q)) =
-                  pack8(dv + 8 * q);
-          }
+            *reinterpret_cast<uint4 *>(sm + SC_DT + chunk16(i, 4 * ch + q)) = pack8(dv + 8 * q);
         }
       }
       fence_proxy_async();
       tc_fence_before();
       named_bar(1);
-      if (i == 0) mbar_arrive(bE6);
-      // state update, handed to the next chunk before the outputs are written
-      if (!rs.wait(i == 0, bE7, ph, abort_flag, err, 32, jc)) break;
+      if (tid == 0) mbar_arrive(bE6);
+      // state update, handed to the next chunk
+      if (!rs.wait(tid == 0, bE7, jc & 1, abort_flag, err, 32, jc)) break;
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      {
         float v[32];
-        tmem_ld32(tbase + lane_off + COL_S + 32 * hh, v);
+        tmem_ld32(tbase + lane_off + COL_S + 32 * ch, v);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) Sm[32 * hh + u] = fmaf(gcs, Sm[32 * hh + u], v[u]);
+        for (int u = 0; u < 32; ++u) Sm[u] = fmaf(gcs, Sm[u], v[u]);
       }
 #pragma unroll
-      for (int cj = 0; cj < 8; ++cj)
-        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, cj)) = pack8(Sm + 8 * cj);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, 4 * ch + q)) = pack8(Sm + 8 * q);
       fence_proxy_async();
       tc_fence_before();
       named_bar(1);
-      if (i == 0 && jc + 1 < nch) mbar_arrive(bE4);
-      // outputs: rows 64..127 of X (Q S0) and of O (P D)
-      if (!rs.wait(i == 0, bE8, ph, abort_flag, err, 34, jc)) break;
+      if (tid == 0 && jc + 1 < nch) mbar_arrive(bE4);
+      // this chunk's outputs, while the next chunk's X is computed (the
+      // staging tile is free once thread 0's earlier stores have read it)
+      if (tid == 0) bulk_wait_read();
+      if (!rs.wait(tid == 0, &bE8[jc & 1], (jc >> 1) & 1, abort_flag, err, 34, jc)) break;
       tc_fence_after();
-      if (warp >= 2) {
-        const int r = i - CH;
-        float *orow = out + ((long long)(t0 + r) * H + h) * DV + NV * vs;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float xv[32], ov[32];
-          tmem_ld32(tbase + lane_off + colx + 32 * hh, xv);
-          tmem_ld32(tbase + lane_off + colo + 32 * hh, ov);
-          if (r < len) {
-            float4 *dst = reinterpret_cast<float4 *>(orow + 32 * hh);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              dst[u] = make_float4(scale * fmaf(qf, xv[4 * u], ov[4 * u]),
-                                   scale * fmaf(qf, xv[4 * u + 1], ov[4 * u + 1]),
-                                   scale * fmaf(qf, xv[4 * u + 2], ov[4 * u + 2]),
-                                   scale * fmaf(qf, xv[4 * u + 3], ov[4 * u + 3]));
-          }
-        }
-      }
+      store_out(jc, qf);
       tc_fence_before();
     }
+    if (tid == 0) bulk_wait_all();
     if (!*abort_flag) {  // state after the chunked part, read by the tail
-      float4 *dst = reinterpret_cast<float4 *>(w.states +
-                                               (((long long)s * H + h) * DK + i) * DV + NV * vs);
+      float4 *dst = reinterpret_cast<float4 *>(
+          w.states + (((long long)s * H + h) * DK + i) * DV + NV * vs + 32 * ch);
 #pragma unroll
-      for (int e = 0; e < NV / 4; ++e)
+      for (int e = 0; e < 8; ++e)
         dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tmem_dealloc(tbase, 512);
   }
@@ -1024,6 +1127,17 @@ bool map_rows(CUtensorMap *m, const void *base, long long rows, int width) {
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 [Ntok][H][D] viewed as (D, H, Ntok); 32 x 1 x 64 boxes, 128-byte swizzle
+bool map_out_f32(CUtensorMap *m, void *base, int ntok, int H, int D) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)ntok};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  const cuuint32_t box[3] = {32, 1, 64}, es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1081,14 +1195,15 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (a.total_tokens > 0) {
-    CUtensorMap mq, mk, mv, mT, mP, mW, mQh, mKt;
+    CUtensorMap mq, mk, mv, mT, mP, mW, mQh, mKt, mo;
     const long long trows = lay.max_chunks * a.H * CH;
     if (trows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are int32
     if (!map_tokens(&mq, a.q, a.total_tokens, a.H, a.Dk) ||
         !map_tokens(&mk, a.k, a.total_tokens, a.H, a.Dk) ||
         !map_tokens(&mv, a.v, a.total_tokens, a.H, a.Dv) ||
         !map_rows(&mT, w.T, trows, CH) || !map_rows(&mP, w.P, trows, CH) ||
-        !map_rows(&mW, w.W, trows, a.Dk))
+        !map_rows(&mW, w.W, trows, a.Dk) ||
+        !map_out_f32(&mo, a.out, a.total_tokens, a.H, a.Dv))
       return cudaErrorInvalidValue;
     if (a.kda && (!map_rows(&mQh, w.Qh, trows, a.Dk) || !map_rows(&mKt, w.Kt, trows, a.Dk)))
       return cudaErrorInvalidValue;
@@ -1103,10 +1218,10 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
     if (a.kda)
       chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, a.scale, w, a.err);
     else
       chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, a.scale, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
