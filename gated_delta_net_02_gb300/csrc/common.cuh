@@ -100,6 +100,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   return false;
 }
 
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy accesses (TMA copies and stores, tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- bulk copies (TMA, non-tensor form) ------------------------------------
 
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte

@@ -73,12 +73,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
                : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (tcgen05.mma operands, TMA stores).
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- TMEM allocation (one warp executes these) ------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

@@ -200,3 +200,45 @@ def test_runs_on_a_side_stream(gdn):
         out, slots = gpu_forward(b, stream=s, dev_tensors=d)
     s.synchronize()
     check_against_oracle(b, out, slots)
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n_slots", [1, 3])
+def test_decode_step_bitwise_equals_first_token_of_longer_run(gdn, mode, dtype, n_slots):
+    """A decode step (T = 1, the persistent decode kernel for 128 x 128 heads)
+    must reproduce, bit for bit, token 0 of a T = 2 run from the same state
+    (the tile kernel): the per-token arithmetic is shared."""
+    b2 = inputs.make_batch(200 + n_slots, [2] * 5, 3, 128, 128, dtype=dtype, mode=mode,
+                           n_slots=2)
+    d2 = to_dev(b2)
+    out2, slots2 = gpu_forward(b2, dev_tensors=d2)
+    first = [2 * s for s in range(5)]
+    b1 = inputs.GDNBatch(b2.q[first], b2.k[first], b2.v[first], b2.g[first], b2.beta[first],
+                         b2.state, mode, b2.scale, torch.ones(5, dtype=torch.int64), n_slots)
+    d1 = {n: t[first] if n != "state" else t for n, t in d2.items()}
+    out1, slots1 = gpu_forward(b1, dev_tensors={n: t.contiguous() for n, t in d1.items()})
+    assert torch.equal(out1, out2[first])
+    assert torch.equal(slots1[:, -1], slots2[:, 0])
+    if n_slots > 1:  # a single token writes only the last slot
+        assert torch.isnan(slots1[:, :-1]).all()
+
+
+def test_decode_step_null_state_and_few_items(gdn):
+    # 1 sequence x 1 head: fewer work items than persistent CTAs; NULL state
+    b = inputs.make_batch(210, [1], 1, 128, 128, state_std=0.0, n_slots=1)
+    out_a, sl_a = gpu_forward(b)
+    out_b, sl_b = gpu_forward(b, state_ptrs=gdn.state_ptr_array([0], "cuda"))
+    assert torch.equal(out_a, out_b) and torch.equal(sl_a, sl_b)
+    check_against_oracle(b, out_a, sl_a)
+
+
+def test_decode_step_state_in_inside_slots_is_refused(gdn):
+    b = inputs.make_batch(211, [1] * 2, 2, 128, 128, n_slots=2)
+    slots = torch.zeros(2, 2, 2, 128, 128, device="cuda")
+    ptrs = gdn.state_ptr_array([slots[1, 0].data_ptr(), 0], "cuda")
+    gpu_forward(b, state_ptrs=ptrs, slots=slots, check=False)
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_check_device_error()
+    assert e.value.status == gdn.GDN_ERR_DEVICE_ARG
+    gdn.gdn_check_device_error()
