@@ -367,12 +367,15 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     __nv_bfloat16 *kt = w.Kt + tile * CH * DK + i;
     float gam = half ? hsum[i] : 0.f;
     float gabs = fabsf(gC);
+    const float eC = __expf(gC);
 #pragma unroll
     for (int rr = 0; rr < HR; ++rr) {
       const int r = r0 + rr;
       gam += gcol[rr];
       gabs = fmaxf(gabs, fabsf(gam));
-      const float e1 = __expf(gam), e2 = __expf(-gam), e3 = __expf(gC - gam);
+      // |gamma| <= 80 inside a chunk (checked below), so e^gC e^-gamma does
+      // not overflow and stands in for e^(gC - gamma)
+      const float e1 = __expf(gam), e2 = __expf(-gam), e3 = eC * e2;
       __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63));
       __nv_bfloat16 *pq =
           reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(CH + r, i & 63));
@@ -500,8 +503,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
     float acc[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    // X is lower triangular: for columns 32..63 (warps with cc >= 32) the
+    // blocks R = 0, 1 are zero and contribute nothing to later blocks
+    const int kb_lo = cc >= 32 ? 2 : 0;
     for (int kb = 0; kb < 4; ++kb) {
-      if (R == kb) {  // finish block R, right-looking
+      if (R == kb && R < kb_lo) {  // an all-zero block of this column
+#pragma unroll
+        for (int u = 0; u < 16; ++u) Xs[(16 * R + u) * XS_LD + cc] = 0.f;
+      } else if (R == kb) {  // finish block R, right-looking
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const float xu = (16 * R + u == cc ? 1.f : 0.f) - acc[u];
@@ -514,7 +523,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
         }
       }
       __syncthreads();
-      if (R > kb) {  // contribution of the finished block kb
+      if (R > kb && kb >= kb_lo) {  // contribution of the finished block kb
 #pragma unroll 1
         for (int k4 = 0; k4 < 4; ++k4) {
           const int k0 = 16 * kb + 4 * k4;
