@@ -626,7 +626,7 @@ def gdn_arm(args, wl_cls):
         kern_s = ms / K / 1e3  # this rank's average launch duration
         achieved = wl.alg_bytes_per_step() / kern_s / 1e9
         if isinstance(wl, Prefill):
-            sha = source_sha("chunked.cu", "umma.cuh", "common.cuh")
+            sha = source_sha("chunked.cu", "recurrent.cu", "umma.cuh", "common.cuh")
             tflops = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
             flops = wl.alg_flops_per_step() / kern_s / 1e12
             roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
