@@ -156,17 +156,6 @@ __global__ void __launch_bounds__(C::NT)
   const long long t0 = p.tok_start ? (long long)p.tok_start[s] : (long long)s * p.T;
   if (T_s <= 0) return;
 
-  const float *Sin = p.state_in[s];
-  if (Sin) {
-    const float *lo = p.slots, *hi = p.slots + p.slots_elems;
-    const float *a = Sin, *b = Sin + (long long)p.H * DK * DV;
-    if (a < hi && b > lo) {  // overlaps the slot buffer: refuse this sequence
-      if (tid == 0) set_error(p.err, kDevOverlap);
-      return;
-    }
-    Sin += (long long)h * DK * DV;
-  }
-
   const int col_base = part * CCOLS;
   const int wcol = col_base + warp * C::WCOLS + cg * 4;  // first column of lane
   const int ntiles = (T_s + TT - 1) / TT;
@@ -205,8 +194,37 @@ __global__ void __launch_bounds__(C::NT)
                  DK * 4, &bar[b]);
     }
   };
+  // gate and beta scalars of a tile (the GDA gate is one value per token),
+  // loaded into registers ahead of the tile's wait
+  auto gate_scalars = [&](int tile, float &gv, float &bv) {
+    const int n = min(TT, T_s - tile * TT);
+    gv = 0.f;
+    bv = 0.f;
+    if (tid < n) {
+      const long long row = (t0 + tile * TT + tid) * p.H + h;
+      if constexpr (!C::KDA) gv = p.g[row];
+      bv = p.beta[row];
+    }
+  };
 
+  // token copies and gate scalars first, then the state pointer
   if (warp == 0) issue(0, 0);
+  float g_cur, b_cur;
+  gate_scalars(0, g_cur, b_cur);
+
+  const float *Sin = p.state_in[s];
+  if (Sin) {
+    const float *lo = p.slots, *hi = p.slots + p.slots_elems;
+    const float *a = Sin, *b = Sin + (long long)p.H * DK * DV;
+    if (a < hi && b > lo) {  // overlaps the slot buffer: refuse this sequence
+      if (tid == 0) {
+        set_error(p.err, kDevOverlap);
+        mbar_wait(&bar[0], 0, nullptr);  // the first tile's copies land before exit
+      }
+      return;
+    }
+    Sin += (long long)h * DK * DV;
+  }
 
   // State slice into registers: st[m] = S[rg + ROWG*m][wcol .. wcol+3].
   float4 st[RPT];
@@ -228,13 +246,15 @@ __global__ void __launch_bounds__(C::NT)
     const uint32_t parity = (tile >> 1) & 1;
     const int n = min(TT, T_s - tile * TT);
     if (warp == 0 && tile + 1 < ntiles) issue(tile + 1, b ^ 1);
+    float g_nxt = 0.f, b_nxt = 0.f;
+    if (tile + 1 < ntiles) gate_scalars(tile + 1, g_nxt, b_nxt);
     if (tid == 0 && !mbar_wait(&bar[b], parity, p.err, 3)) abort_flag = 1;
-    // gate and beta scalars of this tile (GDA gate is one value per token)
     if (tid < n) {
-      const long long row = (t0 + tile * TT + tid) * p.H + h;
-      if constexpr (!C::KDA) fa[tid] = expf(p.g[row]);
-      fb[tid] = p.beta[row];
+      if constexpr (!C::KDA) fa[tid] = expf(g_cur);
+      fb[tid] = b_cur;
     }
+    g_cur = g_nxt;
+    b_cur = b_nxt;
     __syncthreads();
     if (abort_flag) {
       // Let a copy still in flight for the next tile land before exiting.
