@@ -79,7 +79,17 @@ extern "C" {
 
 const char *gdn_last_error(void) { return g_msg.c_str(); }
 
-const char *gdn_version(void) { return "libgdn 0.1.0 (sm_103a)"; }
+const char *gdn_version(void) { return "libgdn 0.2.0 (sm_103a)"; }
+
+// Resolves the grouped-query fields: H_qk = 0 means H; H_qk must divide H.
+static gdn_status qk_heads(const char *fn, int H, int H_qk, int qk_map, int *hq) {
+  *hq = H_qk == 0 ? H : H_qk;
+  if (*hq <= 0 || *hq > H || H % *hq != 0)
+    return fail(GDN_ERR_INVALID_ARG, "%s: H_qk=%d must divide H=%d", fn, H_qk, H);
+  if (qk_map != GDN_QK_TILED && qk_map != GDN_QK_GROUPED)
+    return fail(GDN_ERR_INVALID_ARG, "%s: qk_map %d", fn, qk_map);
+  return GDN_OK;
+}
 
 gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
                        const void *v, const float *g, const float *beta,
@@ -103,6 +113,8 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
                 s.D_k, s.D_v);
   if (!std::isfinite(s.scale))
     return fail(GDN_ERR_INVALID_ARG, "gdn_forward: scale is not finite");
+  int hq = 0;
+  if (qk_heads("gdn_forward", s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
   const long long ntok = (long long)s.n_seqs * s.T;
   if (ntok > (1LL << 31) / s.H)
     return fail(GDN_ERR_UNSUPPORTED, "gdn_forward: %lld tokens x %d heads too large", ntok, s.H);
@@ -128,6 +140,7 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
   a.state_in = state_in; a.slots = state_slots; a.out = out;
   a.tok_start = nullptr; a.seq_len = nullptr;
   a.n_seqs = s.n_seqs; a.T = s.T; a.H = s.H; a.Dk = s.D_k; a.Dv = s.D_v;
+  a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
   a.n_slots = n_slots;
   a.kda = mode == GDN_MODE_KDA;
   a.bf16 = s.in_dtype == GDN_BF16;
@@ -172,6 +185,9 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
                 "gdn_forward_chunked: bf16 inputs only (fp32 inputs: use gdn_forward)");
   if (!std::isfinite(s.scale))
     return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: scale is not finite");
+  int hq = 0;
+  if (qk_heads("gdn_forward_chunked", s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK)
+    return GDN_ERR_INVALID_ARG;
   if ((long long)s.total_tokens * s.H > (1LL << 31))
     return fail(GDN_ERR_UNSUPPORTED, "gdn_forward_chunked: too many token-heads");
   const void *ptrs[] = {cu_seqlens, state_in, state_slots, workspace};
@@ -204,6 +220,7 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.state_in = state_in; a.slots = state_slots; a.out = out;
   a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
+  a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
   a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
   a.kda = mode == GDN_MODE_KDA;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
@@ -241,6 +258,8 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   if (s.in_dtype != GDN_BF16)
     return fail(GDN_ERR_UNSUPPORTED, "%s: bf16 inputs only (fp32 inputs: use gdn_forward)", fn);
   if (!std::isfinite(s.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+  int hq = 0;
+  if (qk_heads(fn, s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
   if ((long long)s.total_tokens * s.H > (1LL << 31))
     return fail(GDN_ERR_UNSUPPORTED, "%s: too many token-heads", fn);
   const void *ptrs[] = {cu_seqlens, state_in, state_slots};
@@ -274,6 +293,7 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.state_in = state_in; a.slots = state_slots; a.out = out;
   a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
+  a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
   a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
   a.kda = mode == GDN_MODE_KDA;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);

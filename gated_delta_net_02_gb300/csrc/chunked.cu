@@ -276,9 +276,11 @@ template <bool KDA>
 __global__ void __launch_bounds__(PREP_THREADS, 3)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
-                      const float *__restrict__ beta, int H, WsPtrs w, int *err) {
+                      const float *__restrict__ beta, int H, int Hqk, int qk_grouped,
+                      WsPtrs w, int *err) {
   constexpr int DK = 128;
   const int c = blockIdx.x / H, h = blockIdx.x % H;
+  const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
   if (c >= w.hdr[0]) return;
   const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
   const long long tile = (long long)c * H + h;
@@ -306,10 +308,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 3)
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_tma, 32768);
-    tma_load_3d(KQ, &map_k, 0, h, t0, bar_tma);
-    tma_load_3d(KQ + 16384, &map_k, 64, h, t0, bar_tma);
-    tma_load_3d(KQ + 8192, &map_q, 0, h, t0, bar_tma);
-    tma_load_3d(KQ + 16384 + 8192, &map_q, 64, h, t0, bar_tma);
+    tma_load_3d(KQ, &map_k, 0, hq, t0, bar_tma);
+    tma_load_3d(KQ + 16384, &map_k, 64, hq, t0, bar_tma);
+    tma_load_3d(KQ + 8192, &map_q, 0, hq, t0, bar_tma);
+    tma_load_3d(KQ + 16384 + 8192, &map_q, 64, hq, t0, bar_tma);
   }
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
   constexpr int HR = CH / 2;  // KDA: thread (i, half) owns channel i, rows HR*half..
@@ -698,10 +700,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_W,
                       const __grid_constant__ CUtensorMap map_out,
                       const float *const *state_in, float *__restrict__ out, int H,
-                      float scale, WsPtrs w, int *err) {
+                      int Hqk, int qk_grouped, float scale, WsPtrs w, int *err) {
   constexpr int DK = 128, DV = 128;
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
+  const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
   const int s = w.order[(blockIdx.x >> 1) / H];
   const int nch = w.seq_nch[s];
   if (nch == 0) return;
@@ -776,10 +779,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
           tma_load_2d(base + ST_WQ + 8192, &map_q, 0, trow, fb);
           tma_load_2d(base + ST_WQ + 16384 + 8192, &map_q, 64, trow, fb);
         } else {  // raw K and Q rows of the packed token tensors
-          tma_load_3d(base + ST_K, &map_k, 0, h, t0, fb);
-          tma_load_3d(base + ST_K + 8192, &map_k, 64, h, t0, fb);
-          tma_load_3d(base + ST_WQ + 8192, &map_q, 0, h, t0, fb);
-          tma_load_3d(base + ST_WQ + 16384 + 8192, &map_q, 64, h, t0, fb);
+          tma_load_3d(base + ST_K, &map_k, 0, hq, t0, fb);
+          tma_load_3d(base + ST_K + 8192, &map_k, 64, hq, t0, fb);
+          tma_load_3d(base + ST_WQ + 8192, &map_q, 0, hq, t0, fb);
+          tma_load_3d(base + ST_WQ + 16384 + 8192, &map_q, 64, hq, t0, fb);
         }
         tma_load_2d(base + ST_WQ, &map_W, 0, trow, fb);
         tma_load_2d(base + ST_WQ + 16384, &map_W, 64, trow, fb);
@@ -795,10 +798,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
             tma_prefetch_2d(&map_q, 0, prow);
             tma_prefetch_2d(&map_q, 64, prow);
           } else {
-            tma_prefetch_3d(&map_k, 0, h, tp);
-            tma_prefetch_3d(&map_k, 64, h, tp);
-            tma_prefetch_3d(&map_q, 0, h, tp);
-            tma_prefetch_3d(&map_q, 64, h, tp);
+            tma_prefetch_3d(&map_k, 0, hq, tp);
+            tma_prefetch_3d(&map_k, 64, hq, tp);
+            tma_prefetch_3d(&map_q, 0, hq, tp);
+            tma_prefetch_3d(&map_q, 64, hq, tp);
           }
           tma_prefetch_2d(&map_W, 0, prow);
           tma_prefetch_2d(&map_W, 64, prow);
@@ -1207,8 +1210,9 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mT, mP, mW, mQh, mKt, mo;
     const long long trows = lay.max_chunks * a.H * CH;
     if (trows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are int32
-    if (!map_tokens(&mq, a.q, a.total_tokens, a.H, a.Dk) ||
-        !map_tokens(&mk, a.k, a.total_tokens, a.H, a.Dk) ||
+    const int Hqk = a.Hqk > 0 ? a.Hqk : a.H;
+    if (!map_tokens(&mq, a.q, a.total_tokens, Hqk, a.Dk) ||
+        !map_tokens(&mk, a.k, a.total_tokens, Hqk, a.Dk) ||
         !map_tokens(&mv, a.v, a.total_tokens, a.H, a.Dv) ||
         !map_rows(&mT, w.T, trows, CH) || !map_rows(&mP, w.P, trows, CH) ||
         !map_rows(&mW, w.W, trows, a.Dk) ||
@@ -1219,18 +1223,20 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     const long long prep_grid = lay.max_chunks * a.H;
     if (a.kda)
       chunk_prep_kernel<true><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          mq, mk, a.g, a.beta, a.H, w, a.err);
+          mq, mk, a.g, a.beta, a.H, Hqk, a.qk_grouped ? 1 : 0, w, a.err);
     else
       chunk_prep_kernel<false><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          mq, mk, a.g, a.beta, a.H, w, a.err);
+          mq, mk, a.g, a.beta, a.H, Hqk, a.qk_grouped ? 1 : 0, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
     if (a.kda)
       chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
+          a.scale, w, a.err);
     else
       chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, a.scale, w, a.err);
+          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
+          a.scale, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
@@ -1241,6 +1247,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   r.slots = a.slots; r.out = a.out;
   r.tok_start = w.tail_start; r.seq_len = w.tail_len;
   r.n_seqs = a.n_seqs; r.T = 0; r.H = a.H; r.Dk = a.Dk; r.Dv = a.Dv;
+  r.Hqk = a.Hqk > 0 ? a.Hqk : a.H; r.qk_grouped = a.qk_grouped;
   r.n_slots = a.n_slots; r.kda = a.kda; r.bf16 = true; r.scale = a.scale; r.err = a.err;
   return launch_recurrent(r, stream);
 }

@@ -10,7 +10,7 @@ namespace gdn {
 
 // Recurrent (token-loop) forward over n_seqs sequences of one head group.
 struct RecurrentArgs {
-  const void *q, *k, *v;        // [Ntok][H][Dk|Dv], bf16 or fp32
+  const void *q, *k, *v;        // q, k [Ntok][Hqk][Dk]; v [Ntok][H][Dv]; bf16 or fp32
   const float *g, *beta;        // [Ntok][H](x Dk for KDA), [Ntok][H]
   const float *const *state_in; // device [n_seqs] pointers, NULL = zero
   float *slots;                 // [n_seqs][n_slots][H][Dk][Dv]
@@ -18,6 +18,8 @@ struct RecurrentArgs {
   const int *tok_start;         // device [n_seqs] first token, or NULL (s*T)
   const int *seq_len;           // device [n_seqs] tokens, or NULL (T)
   int n_seqs, T, H, Dk, Dv, n_slots;
+  int Hqk;                      // q/k heads (divides H)
+  bool qk_grouped;              // value head h reads q/k head h / (H / Hqk), else h % Hqk
   bool kda, bf16;
   float scale;
   int *err;                     // device error word
@@ -34,6 +36,8 @@ struct ChunkedArgs {
   float *slots;
   float *out;
   int n_seqs, total_tokens, H, Dk, Dv, n_slots;
+  int Hqk;                      // q/k heads (divides H)
+  bool qk_grouped;              // value head -> q/k head map (see RecurrentArgs)
   bool kda;
   float scale;
   void *workspace;

@@ -40,6 +40,7 @@ struct RecParams {
   const int *tok_start, *seq_len;
   long long slots_elems;
   int n_seqs, T, H, n_slots;
+  int Hqk, qk_grouped;  // q/k heads and the value-head -> q/k-head map
   float scale;
   int *err;
 };
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(C::NT)
   const int h = sh % p.H;
   const int s = sh / p.H;
   if (s >= p.n_seqs) return;
+  const int hq = p.qk_grouped ? h / (p.H / p.Hqk) : h % p.Hqk;  // q/k head of h
   const int T_s = p.seq_len ? p.seq_len[s] : p.T;
   const long long t0 = p.tok_start ? (long long)p.tok_start[s] : (long long)s * p.T;
   if (T_s <= 0) return;
@@ -184,8 +186,9 @@ __global__ void __launch_bounds__(C::NT)
     __syncwarp();
     if (lane < n) {
       const long long row = (t0 + tile * TT + lane) * p.H + h;
-      bulk_g2s(rb + lane * DK * sizeof(Tin), q + row * DK, DK * sizeof(Tin), &bar[b]);
-      bulk_g2s(rb + C::RAW_QK + lane * DK * sizeof(Tin), k + row * DK,
+      const long long row_qk = (t0 + tile * TT + lane) * p.Hqk + hq;
+      bulk_g2s(rb + lane * DK * sizeof(Tin), q + row_qk * DK, DK * sizeof(Tin), &bar[b]);
+      bulk_g2s(rb + C::RAW_QK + lane * DK * sizeof(Tin), k + row_qk * DK,
                DK * sizeof(Tin), &bar[b]);
       bulk_g2s(rb + 2 * C::RAW_QK + lane * CCOLS * sizeof(Tin),
                v + row * DV + col_base, CCOLS * sizeof(Tin), &bar[b]);
@@ -348,6 +351,8 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
   p.tok_start = a.tok_start; p.seq_len = a.seq_len;
   p.slots_elems = (long long)a.n_seqs * a.n_slots * a.H * a.Dk * a.Dv;
   p.n_seqs = a.n_seqs; p.T = a.T; p.H = a.H; p.n_slots = a.n_slots;
+  p.Hqk = a.Hqk > 0 ? a.Hqk : a.H;
+  p.qk_grouped = a.qk_grouped ? 1 : 0;
   p.scale = a.scale; p.err = a.err;
   if (a.Dk == 128 && a.Dv == 128) return launch_d<128, 128>(p, a.kda, a.bf16, stream);
   if (a.Dk == 128 && a.Dv == 64) return launch_d<128, 64>(p, a.kda, a.bf16, stream);

@@ -35,16 +35,23 @@ class GDNError(RuntimeError):
         self.status = status
 
 
+GDN_QK_TILED, GDN_QK_GROUPED = 0, 1
+QK_MAPS = {"tiled": GDN_QK_TILED, "grouped": GDN_QK_GROUPED}
+
+
 class gdn_shape(ctypes.Structure):
+    # H_qk = 0 (the default) means q and k have H heads
     _fields_ = [("n_seqs", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("D_k", ctypes.c_int), ("D_v", ctypes.c_int),
-                ("in_dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("in_dtype", ctypes.c_int), ("scale", ctypes.c_float),
+                ("H_qk", ctypes.c_int), ("qk_map", ctypes.c_int)]
 
 
 class gdn_varlen_shape(ctypes.Structure):
     _fields_ = [("n_seqs", ctypes.c_int), ("total_tokens", ctypes.c_int),
                 ("H", ctypes.c_int), ("D_k", ctypes.c_int), ("D_v", ctypes.c_int),
-                ("in_dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("in_dtype", ctypes.c_int), ("scale", ctypes.c_float),
+                ("H_qk", ctypes.c_int), ("qk_map", ctypes.c_int)]
 
 
 if not os.path.exists(LIB_PATH):

@@ -24,8 +24,8 @@ import torch
 
 @dataclass
 class GDNBatch:
-    q: torch.Tensor            # [Ntok, H, Dk]
-    k: torch.Tensor            # [Ntok, H, Dk]
+    q: torch.Tensor            # [Ntok, H_qk, Dk] (H_qk = H unless grouped-query)
+    k: torch.Tensor            # [Ntok, H_qk, Dk]
     v: torch.Tensor            # [Ntok, H, Dv]
     g: torch.Tensor            # [Ntok, H] or [Ntok, H, Dk], fp32
     beta: torch.Tensor         # [Ntok, H], fp32
@@ -35,6 +35,7 @@ class GDNBatch:
     seq_len: torch.Tensor      # int64 [N]
     n_slots: int = 1
     meta: dict = field(default_factory=dict)
+    qk_map: str = "tiled"      # value head -> q/k head when H_qk < H: "tiled" | "grouped"
 
     @property
     def n_seqs(self) -> int:
@@ -47,9 +48,10 @@ class GDNBatch:
         return cu
 
 
-def _tokens(gen, ntok, H, Dk, Dv, dtype, mode, kda_gate_scale=0.1):
-    q = torch.randn(ntok, H, Dk, generator=gen)
-    k = torch.randn(ntok, H, Dk, generator=gen)
+def _tokens(gen, ntok, H, Dk, Dv, dtype, mode, kda_gate_scale=0.1, H_qk=None):
+    Hq = H if H_qk is None else H_qk
+    q = torch.randn(ntok, Hq, Dk, generator=gen)
+    k = torch.randn(ntok, Hq, Dk, generator=gen)
     v = torch.randn(ntok, H, Dv, generator=gen)
     q = q / q.norm(dim=-1, keepdim=True)
     k = k / k.norm(dim=-1, keepdim=True)
@@ -75,18 +77,22 @@ def _state(gen, N, H, Dk, Dv, std):
 def make_batch(seed: int, seq_len, H: int, Dk: int, Dv: int, *,
                dtype=torch.bfloat16, mode: str = "gda", state_std: float = 0.05,
                n_slots: int = 1, scale: Optional[float] = None,
-               kda_gate_scale: float = 0.1) -> GDNBatch:
-    """A packed batch of len(seq_len) sequences drawn with the recipe above."""
+               kda_gate_scale: float = 0.1, H_qk: Optional[int] = None,
+               qk_map: str = "tiled") -> GDNBatch:
+    """A packed batch of len(seq_len) sequences drawn with the recipe above.
+    H_qk < H gives q and k H_qk heads (grouped-query layout, read per value
+    head through qk_map)."""
     gen = torch.Generator("cpu")
     gen.manual_seed(seed)
     seq_len = torch.as_tensor(seq_len, dtype=torch.int64)
     N = int(seq_len.numel())
     ntok = int(seq_len.sum())
     state = _state(gen, N, H, Dk, Dv, state_std)
-    q, k, v, g, beta = _tokens(gen, ntok, H, Dk, Dv, dtype, mode, kda_gate_scale)
+    q, k, v, g, beta = _tokens(gen, ntok, H, Dk, Dv, dtype, mode, kda_gate_scale, H_qk)
     if scale is None:
         scale = Dk ** -0.5
-    return GDNBatch(q, k, v, g, beta, state, mode, float(scale), seq_len, n_slots)
+    return GDNBatch(q, k, v, g, beta, state, mode, float(scale), seq_len, n_slots,
+                    qk_map=qk_map)
 
 
 # ---- the five workloads ---------------------------------------------------

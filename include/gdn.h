@@ -68,6 +68,16 @@ typedef enum {
 typedef enum { GDN_MODE_GDA = 0, GDN_MODE_KDA = 1 } gdn_mode;
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
+/* Grouped-query heads: q and k may carry H_qk heads for H value heads (H a
+ * multiple of H_qk), and the op reads them per value head instead of the
+ * caller repeating them ("models : avoid Q and K repeats when using fused
+ * GDA", llama.cpp commits page, tag b9752). Value head h reads q/k head
+ *   GDN_QK_TILED:   h % H_qk            (heads repeated as a whole block)
+ *   GDN_QK_GROUPED: h / (H / H_qk)      (each q/k head repeated in place)
+ * Both orders occur ("reorder v heads for linear attention to avoid
+ * expensive interleaved repeat", same page, "support qwen3.5 series"). */
+typedef enum { GDN_QK_TILED = 0, GDN_QK_GROUPED = 1 } gdn_qk_map;
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char *gdn_last_error(void);
 
@@ -81,14 +91,16 @@ const char *gdn_version(void);
 typedef struct {
   int n_seqs;         /* N >= 0 independent sequences */
   int T;              /* tokens per sequence, >= 0 */
-  int H;              /* heads (q, k, v all have H heads) */
+  int H;              /* value heads (v, g, beta, out and the state have H heads) */
   int D_k, D_v;       /* head sizes, each 64 or 128 */
   gdn_dtype in_dtype; /* dtype of q, k, v; g and beta are always fp32 */
   float scale;        /* output scale; 0 means 1/sqrt(D_k) */
+  int H_qk;           /* heads of q and k; 0 means H; must divide H */
+  gdn_qk_map qk_map;  /* value head -> q/k head when H_qk < H */
 } gdn_shape;
 
 /*
- * q, k        device [N*T][H][D_k]  in_dtype   (token n*T+t is token t of seq n)
+ * q, k        device [N*T][H_qk][D_k]  in_dtype (token n*T+t is token t of seq n)
  * v           device [N*T][H][D_v]  in_dtype
  * g           device fp32 [N*T][H] (GDA) or [N*T][H][D_k] (KDA)
  * beta        device fp32 [N*T][H]
@@ -123,10 +135,12 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
 typedef struct {
   int n_seqs;         /* N >= 1 */
   int total_tokens;   /* Ntok = cu_seqlens[N] */
-  int H;
+  int H;              /* value heads */
   int D_k, D_v;       /* D_k = D_v = 128 for the tensor-core path */
   gdn_dtype in_dtype; /* GDN_BF16 (fp32 inputs use gdn_forward per sequence) */
   float scale;        /* 0 means 1/sqrt(D_k) */
+  int H_qk;           /* heads of q and k; 0 means H; must divide H */
+  gdn_qk_map qk_map;  /* value head -> q/k head when H_qk < H */
 } gdn_varlen_shape;
 
 /* Bytes of device workspace gdn_forward_chunked needs for this shape in either
@@ -136,7 +150,8 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots);
 /*
  * cu_seqlens  device int32 [N+1], non-decreasing, cu_seqlens[0] = 0,
  *             cu_seqlens[N] = total_tokens (checked on the device)
- * q, k, v, g, beta, out: as gdn_forward with Ntok = total_tokens
+ * q, k, v, g, beta, out: as gdn_forward with Ntok = total_tokens (q, k with
+ *             H_qk heads)
  * state_in    device array of N device pointers (NULL entry = zero state)
  * state_slots device fp32 [N][n_slots][H][D_k][D_v]
  * workspace   device buffer of at least gdn_chunked_workspace_size bytes,

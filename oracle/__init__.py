@@ -59,11 +59,30 @@ class RollbackRangeError(ValueError):
     """The accepted prefix ends at a token whose state was not snapshotted."""
 
 
+def qk_head_index(H, H_qk, qk_map="tiled"):
+    """Which q/k head each of the H value heads reads when q and k carry
+    H_qk <= H heads (grouped-query layout: the op broadcasts q and k instead
+    of the caller repeating them, "models : avoid Q and K repeats when using
+    fused GDA", llama.cpp commits page, tag b9752). Two head orders exist
+    ("reorder v heads for linear attention to avoid expensive interleaved
+    repeat", same page, "support qwen3.5 series"): "tiled" reads head
+    h mod H_qk, "grouped" reads head h // (H // H_qk)."""
+    if H_qk <= 0 or H % H_qk:
+        raise ValueError(f"H={H} is not a multiple of H_qk={H_qk}")
+    h = np.arange(H)
+    if qk_map == "tiled":
+        return h % H_qk
+    if qk_map == "grouped":
+        return h // (H // H_qk)
+    raise ValueError(f"qk_map {qk_map!r}")
+
+
 def forward(q, k, v, g, beta, state_in, *, mode="gda", scale=None, n_slots=0,
-            seq_start=None, seq_len=None, threads=0, want_state=True):
+            seq_start=None, seq_len=None, threads=0, want_state=True, qk_map="tiled"):
     """Runs the token recurrence in fp64.
 
-    q, k: [Ntok, H, Dk]; v: [Ntok, H, Dv]; g: [Ntok, H] (gda) or
+    q, k: [Ntok, H_qk, Dk] with H_qk dividing H (value head h reads q/k head
+    qk_head_index(H, H_qk, qk_map)[h]); v: [Ntok, H, Dv]; g: [Ntok, H] (gda) or
     [Ntok, H, Dk] (kda); beta: [Ntok, H]; state_in: [N, H, Dk, Dv].
     Sequences are either uniform (seq_start/seq_len omitted: N equal runs of
     Ntok/N tokens) or given by seq_start/seq_len (int64 [N]).
@@ -74,6 +93,10 @@ def forward(q, k, v, g, beta, state_in, *, mode="gda", scale=None, n_slots=0,
     """
     q, k, v = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
     g, beta, state_in = _f64(g, "g"), _f64(beta, "beta"), _f64(state_in, "state_in")
+    if q.shape[1] != v.shape[1]:  # broadcast the q/k heads to the value heads
+        idx = qk_head_index(v.shape[1], q.shape[1], qk_map)
+        q = np.ascontiguousarray(q[:, idx])
+        k = np.ascontiguousarray(k[:, idx])
     ntok, H, Dk = q.shape
     Dv = v.shape[2]
     N = state_in.shape[0]
@@ -120,4 +143,4 @@ def rollback_slot(T: int, K: int, n_accepted: int) -> int:
     return slot.value
 
 
-__all__ = ["forward", "rollback_slot", "max_threads", "RollbackRangeError"]
+__all__ = ["forward", "rollback_slot", "max_threads", "qk_head_index", "RollbackRangeError"]

@@ -27,7 +27,8 @@ def oracle_run(b: inputs.GDNBatch, n_slots=None, threads=0):
     return oracle.forward(
         inputs.to_f64(b.q), inputs.to_f64(b.k), inputs.to_f64(b.v), inputs.to_f64(b.g),
         inputs.to_f64(b.beta), inputs.to_f64(b.state), mode=b.mode, scale=b.scale,
-        n_slots=n_slots, seq_start=cu[:-1], seq_len=b.seq_len.numpy(), threads=threads)
+        n_slots=n_slots, seq_start=cu[:-1], seq_len=b.seq_len.numpy(), threads=threads,
+        qk_map=b.qk_map)
 
 
 def to_dev(b: inputs.GDNBatch, dev="cuda"):
@@ -45,7 +46,7 @@ def gpu_forward(b: inputs.GDNBatch, n_slots=None, state_ptrs=None, slots=None,
     T = int(b.seq_len[0]) if N else 0
     assert bool((b.seq_len == T).all()), "gdn_forward needs uniform lengths"
     d = dev_tensors or to_dev(b)
-    H, Dk = b.q.shape[1], b.q.shape[2]
+    H, Dk = b.v.shape[1], b.q.shape[2]
     Dv = b.v.shape[2]
     if slots is None:
         slots = torch.full((N, n_slots, H, Dk, Dv), float("nan"), device="cuda")
@@ -53,7 +54,8 @@ def gpu_forward(b: inputs.GDNBatch, n_slots=None, state_ptrs=None, slots=None,
         out = torch.full((N * T, H, Dv), float("nan"), device="cuda")
     if state_ptrs is None:
         state_ptrs = gdn.state_ptr_array(gdn.per_seq_state_ptrs(d["state"], N), "cuda")
-    shape = gdn.gdn_shape(N, T, H, Dk, Dv, gdn.dtype_code(b.q.dtype), b.scale)
+    shape = gdn.gdn_shape(N, T, H, Dk, Dv, gdn.dtype_code(b.q.dtype), b.scale,
+                          b.q.shape[1], gdn.QK_MAPS[b.qk_map])
     gdn.gdn_forward(shape, d["q"], d["k"], d["v"], d["g"], d["beta"], state_ptrs, slots, out,
                     n_slots, b.mode, stream)
     if check:

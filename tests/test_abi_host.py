@@ -169,3 +169,19 @@ def test_slot_state_ptr_arithmetic(gdn):
     assert gdn.gdn_slot_state_ptr(base, 2, -1, K, H, Dk, Dv) == 0
     with pytest.raises(gdn.GDNError):
         gdn.gdn_slot_state_ptr(base, 0, K, K, H, Dk, Dv)
+
+
+def test_grouped_query_heads_are_validated_on_the_host(gdn):
+    # H_qk must divide H (0 means H); qk_map is tiled (0) or grouped (1)
+    assert call_forward(gdn, shape(gdn, H=4, H_qk=3)) == gdn.GDN_ERR_INVALID_ARG
+    assert "H_qk" in gdn.gdn_last_error()
+    assert call_forward(gdn, shape(gdn, H=4, H_qk=8)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, H=4, H_qk=-2)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_forward(gdn, shape(gdn, H=4, H_qk=2, qk_map=5)) == gdn.GDN_ERR_INVALID_ARG
+    assert "qk_map" in gdn.gdn_last_error()
+    assert call_chunked(gdn, vshape(gdn, H=6, H_qk=4)) == gdn.GDN_ERR_INVALID_ARG
+    assert call_chunked(gdn, vshape(gdn, H=6, H_qk=3, qk_map=2)) == gdn.GDN_ERR_INVALID_ARG
+    # valid grouped-query fields pass validation (the next failure is a NULL input)
+    assert call_forward(gdn, shape(gdn, H=4, H_qk=2, qk_map=gdn.GDN_QK_GROUPED), q=0) \
+        == gdn.GDN_ERR_INVALID_ARG
+    assert "q is NULL" in gdn.gdn_last_error()

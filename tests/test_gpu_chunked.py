@@ -30,10 +30,11 @@ def chunked_forward(gdn, b, n_slots=None, state_ptrs=None, cu=None, check=True,
     n_slots = b.n_slots if n_slots is None else n_slots
     d = dev_tensors or to_dev(b)
     N = b.n_seqs
-    H, Dk, Dv = b.q.shape[1], b.q.shape[2], b.v.shape[2]
+    H, Dk, Dv = b.v.shape[1], b.q.shape[2], b.v.shape[2]
     ntok = b.q.shape[0]
     cu_dev = (b.cu_seqlens if cu is None else cu).to(torch.int32).cuda()
-    shape = gdn.gdn_varlen_shape(N, ntok, H, Dk, Dv, gdn.GDN_BF16, b.scale)
+    shape = gdn.gdn_varlen_shape(N, ntok, H, Dk, Dv, gdn.GDN_BF16, b.scale, b.q.shape[1],
+                                 gdn.QK_MAPS[b.qk_map])
     ws_bytes = gdn.gdn_chunked_workspace_size(shape, n_slots)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     slots = torch.full((N, n_slots, H, Dk, Dv), float("nan"), device="cuda")
@@ -160,3 +161,13 @@ def test_kda_decay_beyond_range_reported(gdn):
     o_ref, s_ref, _ = oracle_run(b, n_slots=1)
     assert rel_l2(out.double().cpu().numpy(), o_ref) <= TOL_BF16
     assert rel_l2(slots[:, -1].double().cpu().numpy(), s_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("qk_map", ["tiled", "grouped"])
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+def test_grouped_query_heads(gdn, qk_map, mode):
+    # 4 value heads reading 2 q/k heads, ragged varlen batch with a short tail
+    b = inputs.make_batch(230, [300, 70, 5], 4, 128, 128, mode=mode, n_slots=4, H_qk=2,
+                          qk_map=qk_map)
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)

@@ -242,3 +242,20 @@ def test_decode_step_state_in_inside_slots_is_refused(gdn):
         gdn.gdn_check_device_error()
     assert e.value.status == gdn.GDN_ERR_DEVICE_ARG
     gdn.gdn_check_device_error()
+
+
+@pytest.mark.parametrize("qk_map", ["tiled", "grouped"])
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_grouped_query_heads(gdn, qk_map, mode, dtype):
+    # 6 value heads reading 2 q/k heads; T = 19 spans three token tiles
+    b = inputs.make_batch(220, [19] * 2, 6, 128, 128, dtype=dtype, mode=mode, n_slots=3,
+                          H_qk=2, qk_map=qk_map)
+    out, slots = gpu_forward(b)
+    check_against_oracle(b, out, slots)
+
+
+def test_grouped_query_decode_step(gdn):
+    b = inputs.make_batch(221, [1] * 8, 8, 128, 128, n_slots=1, H_qk=2, qk_map="grouped")
+    out, slots = gpu_forward(b)
+    check_against_oracle(b, out, slots)

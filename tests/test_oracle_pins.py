@@ -386,3 +386,40 @@ def test_empty_sequence_returns_input_state():
     _, S, _ = oracle.forward(q, k, v, g, beta, S0, seq_start=np.array([0, 0]),
                              seq_len=np.array([0, 3]))
     assert np.array_equal(S[0], S0[0])
+
+
+def test_grouped_query_head_maps():
+    # tiled repeats the H_qk heads as a block, grouped repeats each head in place
+    assert oracle.qk_head_index(6, 2, "tiled").tolist() == [0, 1, 0, 1, 0, 1]
+    assert oracle.qk_head_index(6, 2, "grouped").tolist() == [0, 0, 0, 1, 1, 1]
+    assert oracle.qk_head_index(4, 4, "grouped").tolist() == [0, 1, 2, 3]
+    with pytest.raises(ValueError):
+        oracle.qk_head_index(6, 4, "tiled")
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("qk_map,expand", [
+    ("tiled", lambda x, r: np.tile(x, (1, r, 1))),     # the heads as a repeated block
+    ("grouped", lambda x, r: np.repeat(x, r, axis=1)),  # each head repeated in place
+])
+def test_grouped_query_equals_explicitly_repeated_heads(mode, qk_map, expand):
+    """Broadcasting H_qk q/k heads to H value heads equals running the plain
+    op on q, k repeated to H heads by numpy's tile / repeat."""
+    rng = np.random.default_rng(31)
+    ntok, H, Hqk, Dk, Dv = 12, 6, 2, 16, 8
+    q = rng.standard_normal((ntok, Hqk, Dk))
+    k = rng.standard_normal((ntok, Hqk, Dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((ntok, H, Dv))
+    g = -np.log1p(np.exp(rng.standard_normal((ntok, H, Dk) if mode == "kda" else (ntok, H))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((ntok, H))))
+    S0 = 0.05 * rng.standard_normal((2, H, Dk, Dv))
+    kw = dict(mode=mode, n_slots=2, seq_start=np.array([0, 7]), seq_len=np.array([7, 5]))
+    o1, s1, sl1 = oracle.forward(q, k, v, g, beta, S0, qk_map=qk_map, **kw)
+    o2, s2, sl2 = oracle.forward(expand(q, 3), expand(k, 3), v, g, beta, S0, **kw)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+    assert np.array_equal(sl1, sl2, equal_nan=True)
+    # and the two head orders really differ
+    other = "grouped" if qk_map == "tiled" else "tiled"
+    o3, _, _ = oracle.forward(q, k, v, g, beta, S0, qk_map=other, **kw)
+    assert not np.allclose(o1, o3)
