@@ -155,7 +155,7 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots) {
       n_slots < 1)
     return 0;
   return gdn::chunked_workspace_size(shape->n_seqs, shape->total_tokens, shape->H,
-                                     shape->D_k, shape->D_v, n_slots);
+                                     shape->D_k, shape->D_v, shape->in_dtype == GDN_BF16);
 }
 
 gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
@@ -176,13 +176,10 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
     return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: in_dtype %d", (int)s.in_dtype);
   if (n_slots < 1)
     return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: n_slots=%d (need >= 1)", n_slots);
-  if (s.D_k != 128 || s.D_v != 128)
+  if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
     return fail(GDN_ERR_UNSUPPORTED,
-                "gdn_forward_chunked: tensor-core path needs D_k = D_v = 128 (got %d, %d)",
-                s.D_k, s.D_v);
-  if (s.in_dtype != GDN_BF16)
-    return fail(GDN_ERR_UNSUPPORTED,
-                "gdn_forward_chunked: bf16 inputs only (fp32 inputs: use gdn_forward)");
+                "gdn_forward_chunked: head sizes D_k=%d D_v=%d (supported: 64, 128)", s.D_k,
+                s.D_v);
   if (!std::isfinite(s.scale))
     return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: scale is not finite");
   int hq = 0;
@@ -221,6 +218,7 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
   a.state_in = state_in; a.slots = state_slots; a.out = out;
   a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
   a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
+  a.bf16 = s.in_dtype == GDN_BF16;
   a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
   a.kda = mode == GDN_MODE_KDA;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
@@ -252,11 +250,9 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
     return fail(GDN_ERR_INVALID_ARG, "%s: in_dtype %d", fn, (int)s.in_dtype);
   if (n_slots < 1) return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d (need >= 1)", fn, n_slots);
-  if (s.D_k != 128 || s.D_v != 128)
-    return fail(GDN_ERR_UNSUPPORTED, "%s: tensor-core path needs D_k = D_v = 128 (got %d, %d)",
-                fn, s.D_k, s.D_v);
-  if (s.in_dtype != GDN_BF16)
-    return fail(GDN_ERR_UNSUPPORTED, "%s: bf16 inputs only (fp32 inputs: use gdn_forward)", fn);
+  if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
+    return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes D_k=%d D_v=%d (supported: 64, 128)", fn,
+                s.D_k, s.D_v);
   if (!std::isfinite(s.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
   int hq = 0;
   if (qk_heads(fn, s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
@@ -278,7 +274,8 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
     return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
   const size_t need = gdn::chunked_workspace_need(s.n_seqs, s.total_tokens, s.H, s.D_k,
-                                                  s.D_v, mode == GDN_MODE_KDA);
+                                                  s.D_v, mode == GDN_MODE_KDA,
+                                                  s.in_dtype == GDN_BF16);
   if (need > gdn::static_scratch_bytes())
     return fail(GDN_ERR_UNSUPPORTED,
                 "%s: this shape needs %zu bytes of scratch; the built-in area holds %zu "
@@ -294,6 +291,7 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
   a.state_in = state_in; a.slots = state_slots; a.out = out;
   a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
   a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
+  a.bf16 = s.in_dtype == GDN_BF16;
   a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
   a.kda = mode == GDN_MODE_KDA;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);

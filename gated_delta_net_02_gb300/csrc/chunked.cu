@@ -65,9 +65,12 @@ struct WsLayout {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda) {
+// with_tiles = false: the token-loop route (fp32 inputs or head sizes other
+// than 128), which needs only the per-sequence work list.
+WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda,
+                   bool with_tiles = true) {
   WsLayout w{};
-  w.max_chunks = (long long)total_tokens / CH + n_seqs;
+  w.max_chunks = with_tiles ? (long long)total_tokens / CH + n_seqs : 0;
   const size_t tiles = (size_t)w.max_chunks * H;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -85,7 +88,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
   w.tail_len = take(sizeof(int) * (size_t)n_seqs);
   w.order = take(sizeof(int) * (size_t)n_seqs);
   w.state_ptrs = take(sizeof(float *) * (size_t)n_seqs);
-  w.states = take(sizeof(float) * (size_t)n_seqs * H * Dk * Dv);
+  w.states = take(with_tiles ? sizeof(float) * (size_t)n_seqs * H * Dk * Dv : 0);
   w.T = take(2 * tiles * CH * CH);
   w.P = take(2 * tiles * CH * CH);
   w.W = take(2 * tiles * CH * Dk);
@@ -1183,16 +1186,39 @@ cudaError_t set_attributes() {
 
 // The public size query has no gate mode, so it returns the larger (KDA)
 // layout; a GDA call needs less and fits in it.
-size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk, int Dv, int) {
-  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, true).total;
+size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool bf16) {
+  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, true, tensor_core_route(bf16, Dk, Dv)).total;
 }
 
-size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda) {
-  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, kda).total;
+size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda,
+                              bool bf16) {
+  return ws_layout(n_seqs, total_tokens, H, Dk, Dv, kda, tensor_core_route(bf16, Dk, Dv)).total;
+}
+
+// fp32 inputs and head sizes other than 128: every token of every sequence
+// through the recurrent kernel (which also writes the slots), from the work
+// list with no chunked part.
+static cudaError_t launch_token_loop(const ChunkedArgs &a, cudaStream_t stream) {
+  const WsLayout lay = ws_layout(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda, false);
+  if (a.workspace_bytes < lay.total) return cudaErrorInvalidValue;
+  const WsPtrs w = ws_ptrs(a.workspace, lay);
+  worklist_kernel<<<1, WL_THREADS, 0, stream>>>(a.cu_seqlens, a.n_seqs, a.total_tokens,
+                                                0x7fffffff, a.H, 0, a.state_in, w, a.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  RecurrentArgs r{};
+  r.q = a.q; r.k = a.k; r.v = a.v; r.g = a.g; r.beta = a.beta;
+  r.state_in = w.state_ptrs;
+  r.slots = a.slots; r.out = a.out;
+  r.tok_start = w.tail_start; r.seq_len = w.tail_len;
+  r.n_seqs = a.n_seqs; r.T = 0; r.H = a.H; r.Dk = a.Dk; r.Dv = a.Dv;
+  r.Hqk = a.Hqk > 0 ? a.Hqk : a.H; r.qk_grouped = a.qk_grouped;
+  r.n_slots = a.n_slots; r.kda = a.kda; r.bf16 = a.bf16; r.scale = a.scale; r.err = a.err;
+  return launch_recurrent(r, stream);
 }
 
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
-  if (a.Dk != 128 || a.Dv != 128) return cudaErrorInvalidValue;
+  if (!tensor_core_route(a.bf16, a.Dk, a.Dv)) return launch_token_loop(a, stream);
   if (!encode_fn()) return cudaErrorNotSupported;
   cudaError_t e = set_attributes();
   if (e != cudaSuccess) return e;
@@ -1279,7 +1305,7 @@ size_t static_scratch_bytes() { return kStaticScratchBytes; }
 // (and launches nothing) when *need exceeds the static area. The first call
 // on a device looks up the area's device address with that device current.
 cudaError_t launch_chunked_static(ChunkedArgs a, cudaStream_t stream, size_t *need) {
-  *need = chunked_workspace_need(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda);
+  *need = chunked_workspace_need(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda, a.bf16);
   if (*need > kStaticScratchBytes) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -30,7 +30,7 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);
 // Chunked (tensor-core) prefill of varlen sequences; see chunked.cu.
 struct ChunkedArgs {
   const int32_t *cu_seqlens;    // device [n_seqs + 1]
-  const void *q, *k, *v;        // bf16
+  const void *q, *k, *v;        // bf16 (tensor-core route) or fp32
   const float *g, *beta;
   const float *const *state_in; // device [n_seqs]
   float *slots;
@@ -38,6 +38,7 @@ struct ChunkedArgs {
   int n_seqs, total_tokens, H, Dk, Dv, n_slots;
   int Hqk;                      // q/k heads (divides H)
   bool qk_grouped;              // value head -> q/k head map (see RecurrentArgs)
+  bool bf16;                    // q, k, v dtype (else fp32)
   bool kda;
   float scale;
   void *workspace;
@@ -45,10 +46,13 @@ struct ChunkedArgs {
   int *err;
 };
 
-size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk,
-                              int Dv, int n_slots);
+// bf16 inputs with 128 x 128 heads run on the tensor cores; anything else
+// goes through the recurrent kernel, token by token.
+inline bool tensor_core_route(bool bf16, int Dk, int Dv) { return bf16 && Dk == 128 && Dv == 128; }
+size_t chunked_workspace_size(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool bf16);
 // Bytes one call of the given gate mode needs (at most the size above).
-size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda);
+size_t chunked_workspace_need(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda,
+                              bool bf16);
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream);
 
 // The chunked path on the library's fixed scratch area (no workspace

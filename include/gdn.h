@@ -125,19 +125,24 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
 /* ------------------------------------------------------------------------
  * Varlen chunked prefill ("llama : enable chunked fused GDN path", llama.cpp
  * commits, tag b9752). Sequence s covers packed tokens
- * [cu_seqlens[s], cu_seqlens[s+1]). Tokens [0, L_s - n_slots) of each
- * sequence run through the chunked (chunk 64, WY/UT-transform) tensor-core
- * kernels, with the last partial chunk padded by no-op rows; the last
- * n_slots tokens run through the recurrent kernel, which writes the slots.
- * The result equals the token recurrence up to rounding (bf16 tensor-core
- * operands, fp32 accumulation and fp32 state).
+ * [cu_seqlens[s], cu_seqlens[s+1]). Routing:
+ *  - bf16 inputs with D_k = D_v = 128: tokens [0, L_s - n_slots) of each
+ *    sequence run through the chunked (chunk 64, WY/UT-transform)
+ *    tensor-core kernels, with the last partial chunk padded by no-op rows;
+ *    the last n_slots tokens run through the recurrent kernel, which writes
+ *    the slots. The result equals the token recurrence up to rounding (bf16
+ *    tensor-core operands, fp32 accumulation and fp32 state).
+ *  - fp32 inputs (whose 1e-5 accuracy bf16 operands cannot meet) and head
+ *    sizes of 64: every token runs through the recurrent kernel on the GPU,
+ *    as the pages' chunked path also falls back to the token loop ("Enable
+ *    GDN also for prefill, move TODO for chunked_GDN", llama.cpp commits).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int n_seqs;         /* N >= 1 */
   int total_tokens;   /* Ntok = cu_seqlens[N] */
   int H;              /* value heads */
-  int D_k, D_v;       /* D_k = D_v = 128 for the tensor-core path */
-  gdn_dtype in_dtype; /* GDN_BF16 (fp32 inputs use gdn_forward per sequence) */
+  int D_k, D_v;       /* each 64 or 128 */
+  gdn_dtype in_dtype; /* GDN_BF16 or GDN_F32 (see the routing note below) */
   float scale;        /* 0 means 1/sqrt(D_k) */
   int H_qk;           /* heads of q and k; 0 means H; must divide H */
   gdn_qk_map qk_map;  /* value head -> q/k head when H_qk < H */

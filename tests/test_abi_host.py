@@ -105,8 +105,9 @@ def call_chunked(gdn, sh, n_slots=1, ws_bytes=None, **ptrs):
 
 
 def test_chunked_argument_errors(gdn):
-    assert call_chunked(gdn, vshape(gdn, D_k=64, D_v=64)) == gdn.GDN_ERR_UNSUPPORTED
-    assert call_chunked(gdn, vshape(gdn, in_dtype=gdn.GDN_F32)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_chunked(gdn, vshape(gdn, D_k=32)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_chunked(gdn, vshape(gdn, D_v=96)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call_chunked(gdn, vshape(gdn, in_dtype=7)) == gdn.GDN_ERR_INVALID_ARG
     assert call_chunked(gdn, vshape(gdn, n_seqs=0)) == gdn.GDN_ERR_INVALID_ARG
     assert call_chunked(gdn, vshape(gdn), n_slots=0, ws_bytes=1 << 30) == gdn.GDN_ERR_INVALID_ARG
     assert call_chunked(gdn, vshape(gdn), cu=0) == gdn.GDN_ERR_INVALID_ARG

@@ -33,8 +33,8 @@ def chunked_forward(gdn, b, n_slots=None, state_ptrs=None, cu=None, check=True,
     H, Dk, Dv = b.v.shape[1], b.q.shape[2], b.v.shape[2]
     ntok = b.q.shape[0]
     cu_dev = (b.cu_seqlens if cu is None else cu).to(torch.int32).cuda()
-    shape = gdn.gdn_varlen_shape(N, ntok, H, Dk, Dv, gdn.GDN_BF16, b.scale, b.q.shape[1],
-                                 gdn.QK_MAPS[b.qk_map])
+    shape = gdn.gdn_varlen_shape(N, ntok, H, Dk, Dv, gdn.dtype_code(b.q.dtype), b.scale,
+                                 b.q.shape[1], gdn.QK_MAPS[b.qk_map])
     ws_bytes = gdn.gdn_chunked_workspace_size(shape, n_slots)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     slots = torch.full((N, n_slots, H, Dk, Dv), float("nan"), device="cuda")
@@ -171,3 +171,21 @@ def test_grouped_query_heads(gdn, qk_map, mode):
                           qk_map=qk_map)
     out, slots = chunked_forward(gdn, b)
     compare(b, out, slots)
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("dtype,D", [(torch.float32, 128), (torch.float32, 64),
+                                     (torch.bfloat16, 64)])
+def test_token_loop_route(gdn, mode, dtype, D):
+    """fp32 inputs and 64-wide heads take the recurrent kernel for every
+    token: fp32 must then meet the fp32 tolerance."""
+    b = inputs.make_batch(240, [150, 3, 0, 70], 2, D, D, dtype=dtype, mode=mode, n_slots=4)
+    out, slots = chunked_forward(gdn, b)
+    tol = 1e-5 if dtype == torch.float32 else TOL_BF16
+    compare(b, out, slots, tol=tol)
+
+
+def test_token_loop_route_needs_only_the_work_list(gdn):
+    big = gdn.gdn_varlen_shape(8, 40000, 16, 128, 128, gdn.GDN_BF16, 0.0)
+    f32 = gdn.gdn_varlen_shape(8, 40000, 16, 128, 128, gdn.GDN_F32, 0.0)
+    assert gdn.gdn_chunked_workspace_size(f32, 8) < 4096 < gdn.gdn_chunked_workspace_size(big, 8)
