@@ -249,10 +249,11 @@ constexpr int XS_LD = 68;  // fp32 row stride of X (16-byte rows, conflict-free 
 //     64..127 (TMA; KDA scales them in place to K^ = e^g . K and Q^ = e^g . Q).
 //     A of G; its K rows are also B of W. Once G is done the Q rows hold A
 //     (fp32, rows 0..31 in half 0 and rows 32..63 in half 1, see af_off).
-//  TZ [64][64] bf16: T', rows 0..63 of the A operand of W (rows 64..127 of
-//     that operand read the next 8 KB, whose products are never used).
+//  TZ [64][64] bf16: T', written after the solve into the Q rows of half 0
+//     (free by then); rows 0..63 of the A operand of W (rows 64..127 of that
+//     operand read the next 8 KB, K rows, whose products are never used).
 //  KB [64][128] bf16: KDA e^-g . K (B of G); afterwards X fp32 [64][XS_LD].
-constexpr int PREP_KQ = 0, PREP_TZ = 32768, PREP_KB = 40960;
+constexpr int PREP_KQ = 0, PREP_TZ = 8192, PREP_KB = 32768;
 constexpr int PREP_GAM = PREP_KB + 64 * XS_LD * 4;  // [64] f32 gamma (GDA)
 constexpr int PREP_TF = PREP_GAM + 256;             // [64] f32 column factor of T'
 constexpr int PREP_BETA = PREP_TF + 256;            // [64] f32
@@ -276,7 +277,7 @@ __device__ __forceinline__ uint32_t af_off(int r, int j) {
 // One CTA per (chunk, head). Rows r of the chunk are tokens chunk_tok + r,
 // r < len; the rest are padding (k = q = 0, beta = 0, g = 0).
 template <bool KDA>
-__global__ void __launch_bounds__(PREP_THREADS, 3)
+__global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
                       const float *__restrict__ beta, int H, int Hqk, int qk_grouped,
