@@ -50,6 +50,20 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate_over_ranks(ms, ms_e2e, tokens_per_step, K, ws, device):
+    """Whole-job figures of a replicated run: each rank timed K steps of its
+    own replica (ms, ms_e2e); the job's time is the slowest rank's, and its
+    tokens are every rank's. Uses a MAX all-reduce when ws > 1 (any backend).
+    Returns (ms_max, ms_e2e_max, tokens/s, e2e tokens/s)."""
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max, ms_e2e_max = t.tolist()
+    tokens_all = tokens_per_step * K * ws
+    return ms_max, ms_e2e_max, tokens_all / (ms_max / 1e3), tokens_all / (ms_e2e_max / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -654,14 +668,8 @@ def gdn_arm(args, wl_cls):
                             "ping-pongs between two buffers and largely stays in L2; an L2 "
                             "figure beside the cold-L2 headline, not the headline"}
 
-    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max, ms_e2e_max = t.tolist()
-    tokens_all = wl.tokens_per_step * K * ws
-    value = tokens_all / (ms_max / 1e3)
-    e2e_value = tokens_all / (ms_e2e_max / 1e3)
+    ms_max, ms_e2e_max, value, e2e_value = aggregate_over_ranks(
+        ms, ms_e2e, wl.tokens_per_step, K, ws, dev)
 
     if rank == 0:
         peaks, src = measured_peaks()
