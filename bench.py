@@ -407,8 +407,8 @@ class Prefill:
         self.N, self.H = b0.n_seqs, b0.q.shape[1]
         self.ntok = b0.q.shape[0]
         self.K = b0.n_slots
-        self.shape = gdn.gdn_varlen_shape(self.N, self.ntok, self.H, 128, 128, gdn.GDN_BF16,
-                                          b0.scale)
+        self.shape = gdn.gdn_varlen_shape(self.N, self.ntok, self.H, 128, 128,
+                                          gdn.dtype_code(b0.q.dtype), b0.scale)
         self.ws_bytes = gdn.gdn_chunked_workspace_size(self.shape, self.K)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.slots = torch.empty(self.N, self.K, self.H, 128, 128, device=dev)
@@ -423,9 +423,11 @@ class Prefill:
     def tokens_per_step(self):
         return self.ntok
 
+    in_bytes = 2    # q, k, v element size
+
     def alg_bytes_per_step(self):
         g_bytes = 4 * 128 if self.mode == "kda" else 4
-        per_tok_head = 3 * 128 * 2 + g_bytes + 4 + 4 * 128
+        per_tok_head = 3 * 128 * self.in_bytes + g_bytes + 4 + 4 * 128
         state = 2 * self.N * self.H * 128 * 128 * 4 + self.N * self.K * self.H * 128 * 128 * 4
         return per_tok_head * self.ntok * self.H + state
 
@@ -506,7 +508,79 @@ class PrefillVarlen(Prefill):
                 "timing": "CUDA graphs of consecutive calls, CUDA events on the launch stream"}
 
 
+class PrefillVarlenF32(PrefillVarlen):
+    """The varlen batch with fp32 q/k/v: gdn_forward_chunked takes the token
+    loop (the recurrent kernel) for every token."""
+    name = "prefill_varlen_fp32"
+    in_bytes = 4
+
+    def batch(self, j):
+        lens = inputs.varlen_lengths(4)
+        return inputs.make_batch(5 + 100 * j, lens, 16, 128, 128, dtype=torch.float32,
+                                 mode="gda", state_std=0.05, n_slots=8)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("varlen GDA prefill with fp32 q/k/v (token-loop route of "
+                         "gdn_forward_chunked): 8 sequences, lengths ~U[512,8192] (seed 4), "
+                         "H=16, D_k=D_v=128, fp32 state, K=8 slots")
+        c.pop("chunk", None)
+        return c
+
+
+class DecodeGQA(Decode):
+    """The decode step with grouped-query heads: 4 q/k heads read by the 16
+    value heads (grouped map)."""
+    H_QK = 4
+    name = "decode_gqa"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("batched decode with grouped-query heads: 64 sequences x 1 token, "
+                         "H=16 value heads reading H_qk=4 q/k heads (grouped), D_k=D_v=128, "
+                         "GDA, bf16 q/k/v, fp32 state, K=1 slot")
+        c["H_qk"] = self.H_QK
+        return c
+
+    def alg_bytes_per_step(self):
+        D = self.D
+        per_head = 8 * D * D + D * 2 + 4 + 4 + 4 * D       # state r+w, v, g, beta, out
+        return self.N * (self.H * per_head + self.H_QK * 2 * D * 2)
+
+    def setup(self, gdn, dev):
+        super().setup(gdn, dev)
+        hq = self.H_QK
+        for lst in (self.host, self.dev):
+            for i in (0, 1):  # q, k keep their first H_qk heads
+                lst[i] = lst[i][:, :, :hq].contiguous()
+        self.pinned = [h.pin_memory() for h in self.host]
+        self.stage = [torch.empty_like(d[0]) for d in self.dev]
+        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.shape = gdn.gdn_shape(self.N, 1, self.H, self.D, self.D, gdn.GDN_BF16,
+                                   self.D ** -0.5, hq, gdn.GDN_QK_GROUPED)
+
+    def oracle_step_fn(self, n_seqs, threads=0):
+        import oracle
+        N, H, D, hq = self.N, self.H, self.D, self.H_QK
+        st = inputs.to_f64(inputs.decode_state(1, N, H, D)[:n_seqs])
+        pool = []
+        for s_ in range(4):
+            q, k, v, g, beta = (inputs.to_f64(t[:n_seqs]) for t in inputs.decode_tokens(1, s_, N, H, D))
+            pool.append((q[:, :hq].copy(), k[:, :hq].copy(), v, g, beta))
+        state = {"S": st, "i": 0}
+
+        def run():
+            q, k, v, g, beta = pool[state["i"] % len(pool)]
+            _, S, _ = oracle.forward(q, k, v, g, beta, state["S"], scale=D ** -0.5,
+                                     threads=threads, qk_map="grouped")
+            state["S"] = S
+            state["i"] += 1
+            return n_seqs
+        return run
+
+
 WORKLOADS = {"decode": Decode, "verify": Verify, "prefill_kda": PrefillKDA,
+             "decode_gqa": DecodeGQA, "prefill_varlen_fp32": PrefillVarlenF32,
              "prefill_varlen": PrefillVarlen}
 
 
@@ -692,6 +766,11 @@ def gdn_arm(args, wl_cls):
                     # ideal time of the binding roofline / measured time
                     "binding_frac": max(achieved / hbm, flops / tflops),
                     "peak_source": f"{src} hbm_gbs and bf16_tflops"}
+            if wl.in_bytes == 4:  # token-loop route: fp32 CUDA-core work, HBM-bound
+                roof["tensor"] = None
+                roof["binding_frac"] = achieved / hbm
+                roof["kernel"] = "whole gdn_forward_chunked call (token-loop route: work list, " \
+                                 "recurrent kernel)"
         else:
             sha = source_sha("recurrent.cu", "common.cuh")
             roof = None
