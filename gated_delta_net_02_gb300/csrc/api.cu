@@ -158,55 +158,57 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots) {
                                      shape->D_k, shape->D_v, shape->in_dtype == GDN_BF16);
 }
 
-gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
-                               const int32_t *cu_seqlens, const void *q,
-                               const void *k, const void *v, const float *g,
-                               const float *beta, const float *const *state_in,
-                               float *state_slots, float *out, int n_slots,
-                               gdn_mode mode, void *workspace,
-                               size_t workspace_bytes, gdn_stream_t stream) {
-  if (!shape) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: shape is NULL");
+// Validation and launch shared by gdn_forward_chunked (ckpt = NULL) and
+// gdn_forward_chunked_checkpointed.
+static gdn_status chunked_call(const char *fn, const gdn_varlen_shape *shape,
+                               const int32_t *cu_seqlens, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const float *const *state_in, float *state_slots, float *out,
+                               int n_slots, gdn_mode mode, float *ckpt, int ckpt_every,
+                               int max_ckpts, void *workspace, size_t workspace_bytes,
+                               gdn_stream_t stream) {
+  if (!shape) return fail(GDN_ERR_INVALID_ARG, "%s: shape is NULL", fn);
   const gdn_varlen_shape &s = *shape;
   if (s.n_seqs <= 0 || s.total_tokens < 0 || s.H <= 0)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: n_seqs=%d total_tokens=%d H=%d",
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs=%d total_tokens=%d H=%d", fn,
                 s.n_seqs, s.total_tokens, s.H);
   if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: mode %d", (int)mode);
+    return fail(GDN_ERR_INVALID_ARG, "%s: mode %d", fn, (int)mode);
   if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: in_dtype %d", (int)s.in_dtype);
+    return fail(GDN_ERR_INVALID_ARG, "%s: in_dtype %d", fn, (int)s.in_dtype);
   if (n_slots < 1)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: n_slots=%d (need >= 1)", n_slots);
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d (need >= 1)", fn, n_slots);
   if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
     return fail(GDN_ERR_UNSUPPORTED,
-                "gdn_forward_chunked: head sizes D_k=%d D_v=%d (supported: 64, 128)", s.D_k,
+                "%s: head sizes D_k=%d D_v=%d (supported: 64, 128)", fn, s.D_k,
                 s.D_v);
   if (!std::isfinite(s.scale))
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: scale is not finite");
+    return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
   int hq = 0;
-  if (qk_heads("gdn_forward_chunked", s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK)
+  if (qk_heads(fn, s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK)
     return GDN_ERR_INVALID_ARG;
   if ((long long)s.total_tokens * s.H > (1LL << 31))
-    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward_chunked: too many token-heads");
+    return fail(GDN_ERR_UNSUPPORTED, "%s: too many token-heads", fn);
   const void *ptrs[] = {cu_seqlens, state_in, state_slots, workspace};
   const char *names[] = {"cu_seqlens", "state_in", "state_slots", "workspace"};
   for (int i = 0; i < 4; ++i)
-    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is NULL", names[i]);
+    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
   if (s.total_tokens > 0) {
     const void *tp[] = {q, k, v, g, beta, out};
     const char *tn[] = {"q", "k", "v", "g", "beta", "out"};
     for (int i = 0; i < 6; ++i) {
-      if (!tp[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is NULL", tn[i]);
+      if (!tp[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, tn[i]);
       if (!aligned16(tp[i]))
-        return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: %s is not 16-byte aligned", tn[i]);
+        return fail(GDN_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, tn[i]);
     }
   }
   if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: buffers must be 16-byte aligned");
+    return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: workspace must be 256-byte aligned");
+    return fail(GDN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
   const size_t need = gdn_chunked_workspace_size(shape, n_slots);
   if (workspace_bytes < need)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward_chunked: workspace %zu bytes < %zu needed",
+    return fail(GDN_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", fn,
                 workspace_bytes, need);
   int *err = nullptr;
   gdn_status st = device_err_ptr(&err);
@@ -223,9 +225,86 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
   a.kda = mode == GDN_MODE_KDA;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+  a.ckpt = ckpt; a.ckpt_every = ckpt_every; a.max_ckpts = max_ckpts;
   a.err = err;
   return check_launch(gdn::launch_chunked(a, reinterpret_cast<cudaStream_t>(stream)),
-                      "gdn_forward_chunked launch");
+                      fn);
+}
+
+gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
+                               const int32_t *cu_seqlens, const void *q,
+                               const void *k, const void *v, const float *g,
+                               const float *beta, const float *const *state_in,
+                               float *state_slots, float *out, int n_slots,
+                               gdn_mode mode, void *workspace,
+                               size_t workspace_bytes, gdn_stream_t stream) {
+  return chunked_call("gdn_forward_chunked", shape, cu_seqlens, q, k, v, g, beta, state_in,
+                      state_slots, out, n_slots, mode, nullptr, 0, 0, workspace,
+                      workspace_bytes, stream);
+}
+
+static bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+gdn_status gdn_forward_chunked_checkpointed(
+    const gdn_varlen_shape *shape, const int32_t *cu_seqlens, const void *q, const void *k,
+    const void *v, const float *g, const float *beta, const float *const *state_in,
+    float *state_slots, float *out, int n_slots, gdn_mode mode, float *checkpoints,
+    int ckpt_every, int max_ckpts, void *workspace, size_t workspace_bytes,
+    gdn_stream_t stream) {
+  const char *fn = "gdn_forward_chunked_checkpointed";
+  if (!checkpoints) return fail(GDN_ERR_INVALID_ARG, "%s: checkpoints is NULL", fn);
+  if (!aligned16(checkpoints))
+    return fail(GDN_ERR_INVALID_ARG, "%s: checkpoints is not 16-byte aligned", fn);
+  if (ckpt_every <= 0 || ckpt_every % 64 != 0)
+    return fail(GDN_ERR_INVALID_ARG, "%s: ckpt_every=%d (need a positive multiple of 64)", fn,
+                ckpt_every);
+  if (max_ckpts < 1) return fail(GDN_ERR_INVALID_ARG, "%s: max_ckpts=%d (need >= 1)", fn,
+                                 max_ckpts);
+  if (shape && shape->n_seqs > 0 && shape->H > 0 && shape->D_k > 0 && shape->D_v > 0 &&
+      shape->total_tokens >= 0 && n_slots >= 1) {
+    const size_t st = sizeof(float) * (size_t)shape->H * shape->D_k * shape->D_v;
+    const size_t nck = st * (size_t)shape->n_seqs * (size_t)max_ckpts;
+    if (state_slots &&
+        ranges_overlap(checkpoints, nck, state_slots, st * (size_t)shape->n_seqs * n_slots))
+      return fail(GDN_ERR_INVALID_ARG, "%s: checkpoints overlap state_slots", fn);
+    if (out && ranges_overlap(checkpoints, nck, out,
+                              sizeof(float) * (size_t)shape->total_tokens * shape->H *
+                                  shape->D_v))
+      return fail(GDN_ERR_INVALID_ARG, "%s: checkpoints overlap out", fn);
+  }
+  return chunked_call(fn, shape, cu_seqlens, q, k, v, g, beta, state_in, state_slots, out,
+                      n_slots, mode, checkpoints, ckpt_every, max_ckpts, workspace,
+                      workspace_bytes, stream);
+}
+
+gdn_status gdn_checkpoint_select(int n_keep, int L, int n_slots, int ckpt_every,
+                                 int max_ckpts, int *source, int *index, int *replay_from) {
+  const char *fn = "gdn_checkpoint_select";
+  if (!source || !index || !replay_from)
+    return fail(GDN_ERR_INVALID_ARG, "%s: NULL output pointer", fn);
+  if (L < 0 || n_keep < 0 || n_keep > L)
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_keep=%d L=%d (need 0 <= n_keep <= L)", fn, n_keep,
+                L);
+  if (n_slots < 1 || max_ckpts < 1 || ckpt_every <= 0 || ckpt_every % 64 != 0)
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d ckpt_every=%d max_ckpts=%d", fn, n_slots,
+                ckpt_every, max_ckpts);
+  // slot j holds the state after token L - n_slots + j (slots before the
+  // sequence's first token are not written)
+  const int slot = n_keep - 1 - (L - n_slots);
+  if (n_keep >= 1 && slot >= 0) {
+    *source = 2; *index = slot; *replay_from = n_keep;
+    return GDN_OK;
+  }
+  const int m = (n_keep / ckpt_every < max_ckpts ? n_keep / ckpt_every : max_ckpts) - 1;
+  if (m >= 0) {
+    *source = 1; *index = m; *replay_from = (m + 1) * ckpt_every;
+    return GDN_OK;
+  }
+  *source = 0; *index = -1; *replay_from = 0;
+  return GDN_OK;
 }
 
 // Same computation as gdn_forward_chunked, but the scratch it needs lives in

@@ -59,7 +59,7 @@ constexpr int CH = 64;  // chunk length
 
 struct WsLayout {
   size_t hdr, chunk_seq, chunk_tok, chunk_len, seq_chunk0, seq_nch, tail_start,
-      tail_len, order, state_ptrs, states, T, P, W, Qh, Kt, gs, total;
+      tail_len, tail_pos, order, state_ptrs, states, T, P, W, Qh, Kt, gs, total;
   long long max_chunks;
 };
 
@@ -86,6 +86,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
   w.seq_nch = take(sizeof(int) * (size_t)n_seqs);
   w.tail_start = take(sizeof(int) * (size_t)n_seqs);
   w.tail_len = take(sizeof(int) * (size_t)n_seqs);
+  w.tail_pos = take(sizeof(int) * (size_t)n_seqs);
   w.order = take(sizeof(int) * (size_t)n_seqs);
   w.state_ptrs = take(sizeof(float *) * (size_t)n_seqs);
   w.states = take(with_tiles ? sizeof(float) * (size_t)n_seqs * H * Dk * Dv : 0);
@@ -101,7 +102,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
 
 struct WsPtrs {
   int *hdr, *chunk_seq, *chunk_tok, *chunk_len, *seq_chunk0, *seq_nch, *tail_start,
-      *tail_len, *order;
+      *tail_len, *tail_pos, *order;
   const float **state_ptrs;
   float *states;
   __nv_bfloat16 *T, *P, *W, *Qh, *Kt;
@@ -119,6 +120,7 @@ WsPtrs ws_ptrs(void *base, const WsLayout &w) {
   p.seq_nch = reinterpret_cast<int *>(b + w.seq_nch);
   p.tail_start = reinterpret_cast<int *>(b + w.tail_start);
   p.tail_len = reinterpret_cast<int *>(b + w.tail_len);
+  p.tail_pos = reinterpret_cast<int *>(b + w.tail_pos);
   p.order = reinterpret_cast<int *>(b + w.order);
   p.state_ptrs = reinterpret_cast<const float **>(b + w.state_ptrs);
   p.states = reinterpret_cast<float *>(b + w.states);
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(WL_THREADS)
       w.seq_chunk0[s] = 0;
       w.tail_len[s] = 0;
       w.tail_start[s] = 0;
+      w.tail_pos[s] = 0;
       w.order[s] = s;
       w.state_ptrs[s] = nullptr;
     }
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(WL_THREADS)
     w.seq_nch[s] = nch;
     w.tail_start[s] = cu[s] + Lc;
     w.tail_len[s] = L - Lc;
+    w.tail_pos[s] = Lc;  // position of the first tail token within the sequence
     w.state_ptrs[s] = nch > 0 ? w.states + (long long)s * state_elems : state_in[s];
     for (int j = 0; j < nch; ++j) {
       w.chunk_seq[base + j] = s;
@@ -704,7 +708,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_W,
                       const __grid_constant__ CUtensorMap map_out,
                       const float *const *state_in, float *__restrict__ out, int H,
-                      int Hqk, int qk_grouped, float scale, WsPtrs w, int *err) {
+                      int Hqk, int qk_grouped, float scale, WsPtrs w, float *ckpt,
+                      int ckpt_every, int max_ckpts, int *err) {
   constexpr int DK = 128, DV = 128;
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
@@ -1070,6 +1075,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       tc_fence_before();
       named_bar(1);
       if (tid == 0 && jc + 1 < nch) mbar_arrive(bE4);
+      // checkpoint: the state after a full chunk that ends on a multiple of
+      // ckpt_every tokens (chunks start at multiples of 64 in the sequence)
+      if (ckpt && w.chunk_len[chunk0 + jc] == CH) {
+        const int pos = (jc + 1) * CH, c = pos / ckpt_every - 1;
+        if (pos % ckpt_every == 0 && c < max_ckpts) {
+          float4 *dst = reinterpret_cast<float4 *>(
+              ckpt + ((((long long)s * max_ckpts + c) * H + h) * DK + i) * DV + NV * vs +
+              32 * ch);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
+        }
+      }
       // this chunk's outputs, while the next chunk's X is computed (the
       // staging tile is free once thread 0's earlier stores have read it)
       if (tid == 0) bulk_wait_read();
@@ -1215,6 +1233,7 @@ static cudaError_t launch_token_loop(const ChunkedArgs &a, cudaStream_t stream) 
   r.n_seqs = a.n_seqs; r.T = 0; r.H = a.H; r.Dk = a.Dk; r.Dv = a.Dv;
   r.Hqk = a.Hqk > 0 ? a.Hqk : a.H; r.qk_grouped = a.qk_grouped;
   r.n_slots = a.n_slots; r.kda = a.kda; r.bf16 = a.bf16; r.scale = a.scale; r.err = a.err;
+  r.ckpt = a.ckpt; r.pos0 = w.tail_pos; r.ckpt_every = a.ckpt_every; r.max_ckpts = a.max_ckpts;
   return launch_recurrent(r, stream);
 }
 
@@ -1259,11 +1278,11 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     if (a.kda)
       chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
           mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
-          a.scale, w, a.err);
+          a.scale, w, a.ckpt, a.ckpt_every, a.max_ckpts, a.err);
     else
       chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
           mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
-          a.scale, w, a.err);
+          a.scale, w, a.ckpt, a.ckpt_every, a.max_ckpts, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
@@ -1276,6 +1295,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   r.n_seqs = a.n_seqs; r.T = 0; r.H = a.H; r.Dk = a.Dk; r.Dv = a.Dv;
   r.Hqk = a.Hqk > 0 ? a.Hqk : a.H; r.qk_grouped = a.qk_grouped;
   r.n_slots = a.n_slots; r.kda = a.kda; r.bf16 = true; r.scale = a.scale; r.err = a.err;
+  r.ckpt = a.ckpt; r.pos0 = w.tail_pos; r.ckpt_every = a.ckpt_every; r.max_ckpts = a.max_ckpts;
   return launch_recurrent(r, stream);
 }
 

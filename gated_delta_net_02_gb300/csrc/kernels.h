@@ -23,6 +23,11 @@ struct RecurrentArgs {
   bool kda, bf16;
   float scale;
   int *err;                     // device error word
+  // optional checkpoints: the state after sequence position p (1-based count
+  // of tokens) goes to ckpt[s][p / ckpt_every - 1] when p % ckpt_every == 0
+  float *ckpt = nullptr;        // [n_seqs][max_ckpts][H][Dk][Dv]
+  const int *pos0 = nullptr;    // device [n_seqs] position of the first token (NULL = 0)
+  int ckpt_every = 0, max_ckpts = 0;
 };
 
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);
@@ -44,6 +49,8 @@ struct ChunkedArgs {
   void *workspace;
   size_t workspace_bytes;
   int *err;
+  float *ckpt = nullptr;        // optional checkpoints (see RecurrentArgs)
+  int ckpt_every = 0, max_ckpts = 0;
 };
 
 // bf16 inputs with 128 x 128 heads run on the tensor cores; anything else

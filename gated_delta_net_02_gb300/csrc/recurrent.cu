@@ -41,6 +41,9 @@ struct RecParams {
   long long slots_elems;
   int n_seqs, T, H, n_slots;
   int Hqk, qk_grouped;  // q/k heads and the value-head -> q/k-head map
+  float *ckpt;          // optional checkpoints, [n_seqs][max_ckpts][H][Dk][Dv]
+  const int *pos0;      // position of each sequence's first token (NULL = 0)
+  int ckpt_every, max_ckpts;
   float scale;
   int *err;
 };
@@ -128,7 +131,9 @@ __device__ __forceinline__ float4 token_update(float4 (&st)[C::RPT], const float
   return make_float4(o0, o1, o2, o3);
 }
 
-template <class C>
+// CKPT: also store the checkpoints of p.ckpt (a separate instance, so the
+// decode and verify instances carry no trace of it)
+template <class C, bool CKPT>
 __global__ void __launch_bounds__(C::NT)
     recurrent_kernel(const RecParams p) {
   using Tin = typename C::Tin;
@@ -241,6 +246,8 @@ __global__ void __launch_bounds__(C::NT)
   }
 
   const int first_snap = T_s - p.n_slots;  // tokens t >= first_snap are stored
+  int pos0 = 0;
+  if constexpr (CKPT) pos0 = p.pos0 ? p.pos0[s] : 0;
   float *slot_base = p.slots + ((long long)s * p.n_slots * p.H + h) * DK * DV;
   const long long slot_stride = (long long)p.H * DK * DV;
 
@@ -304,6 +311,16 @@ __global__ void __launch_bounds__(C::NT)
 #pragma unroll
         for (int m = 0; m < RPT; ++m) st_f4(dst + (rg + ROWG * m) * DV + wcol, st[m]);
       }
+      // checkpoint at a multiple of ckpt_every tokens of the sequence
+      if constexpr (CKPT) {
+        const int pos = pos0 + t + 1;
+        const int c = pos / p.ckpt_every - 1;
+        if (pos % p.ckpt_every == 0 && c < p.max_ckpts) {
+          float *dst = p.ckpt + (((long long)s * p.max_ckpts + c) * p.H + h) * DK * DV;
+#pragma unroll
+          for (int m = 0; m < RPT; ++m) st_f4(dst + (rg + ROWG * m) * DV + wcol, st[m]);
+        }
+      }
     }
     __syncthreads();  // fp32 tile buffers are rewritten by the next tile
   }
@@ -329,7 +346,10 @@ cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   static_assert(C::SMEM <= 48 * 1024, "fits the default shared-memory window");
-  recurrent_kernel<C><<<(unsigned)n_items, C::NT, C::SMEM, stream>>>(p);
+  if (p.ckpt)
+    recurrent_kernel<C, true><<<(unsigned)n_items, C::NT, C::SMEM, stream>>>(p);
+  else
+    recurrent_kernel<C, false><<<(unsigned)n_items, C::NT, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -353,6 +373,8 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
   p.n_seqs = a.n_seqs; p.T = a.T; p.H = a.H; p.n_slots = a.n_slots;
   p.Hqk = a.Hqk > 0 ? a.Hqk : a.H;
   p.qk_grouped = a.qk_grouped ? 1 : 0;
+  p.ckpt = a.ckpt; p.pos0 = a.pos0;
+  p.ckpt_every = a.ckpt_every > 0 ? a.ckpt_every : 1; p.max_ckpts = a.max_ckpts;
   p.scale = a.scale; p.err = a.err;
   if (a.Dk == 128 && a.Dv == 128) return launch_d<128, 128>(p, a.kda, a.bf16, stream);
   if (a.Dk == 128 && a.Dv == 64) return launch_d<128, 64>(p, a.kda, a.bf16, stream);

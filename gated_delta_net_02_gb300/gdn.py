@@ -77,6 +77,13 @@ lib.gdn_forward_chunked.argtypes = [ctypes.POINTER(gdn_varlen_shape), _vp, _vp, 
 lib.gdn_forward_chunked_noalloc.restype = _st
 lib.gdn_forward_chunked_noalloc.argtypes = [ctypes.POINTER(gdn_varlen_shape), _vp, _vp, _vp,
                                             _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]
+lib.gdn_forward_chunked_checkpointed.restype = _st
+lib.gdn_forward_chunked_checkpointed.argtypes = [
+    ctypes.POINTER(gdn_varlen_shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
+    _vp, _i, _i, _vp, ctypes.c_size_t, _vp]
+lib.gdn_checkpoint_select.restype = _st
+lib.gdn_checkpoint_select.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_i),
+                                      ctypes.POINTER(_i), ctypes.POINTER(_i)]
 lib.gdn_noalloc_scratch_bytes.restype = ctypes.c_size_t
 lib.gdn_noalloc_scratch_bytes.argtypes = []
 lib.gdn_seq_table_create.restype = _st
@@ -156,6 +163,33 @@ def gdn_forward_chunked_noalloc(shape: gdn_varlen_shape, cu_seqlens, q, k, v, g,
                                            _addr(k), _addr(v), _addr(g), _addr(beta),
                                            _addr(state_in), _addr(state_slots), _addr(out),
                                            int(n_slots), _MODES[mode], _stream(stream)))
+
+
+def gdn_forward_chunked_checkpointed(shape: gdn_varlen_shape, cu_seqlens, q, k, v, g, beta,
+                                     state_in, state_slots, out, n_slots: int, mode,
+                                     checkpoints, ckpt_every: int, max_ckpts: int,
+                                     workspace, workspace_bytes: int, stream=None) -> None:
+    """gdn_forward_chunked that also stores checkpoints[s][m], the state
+    after (m+1)*ckpt_every tokens of sequence s (fp32 [N][max_ckpts][H][D_k][D_v])."""
+    _check(lib.gdn_forward_chunked_checkpointed(
+        ctypes.byref(shape), _addr(cu_seqlens), _addr(q), _addr(k), _addr(v), _addr(g),
+        _addr(beta), _addr(state_in), _addr(state_slots), _addr(out), int(n_slots),
+        _MODES[mode], _addr(checkpoints), int(ckpt_every), int(max_ckpts), _addr(workspace),
+        int(workspace_bytes), _stream(stream)))
+
+
+CKPT_SOURCES = ("state_in", "checkpoint", "slot")
+
+
+def gdn_checkpoint_select(n_keep: int, L: int, n_slots: int, ckpt_every: int,
+                          max_ckpts: int):
+    """(source, index, replay_from) for keeping the first n_keep of L tokens;
+    source is one of CKPT_SOURCES."""
+    src, idx, rep = _i(), _i(), _i()
+    _check(lib.gdn_checkpoint_select(int(n_keep), int(L), int(n_slots), int(ckpt_every),
+                                     int(max_ckpts), ctypes.byref(src), ctypes.byref(idx),
+                                     ctypes.byref(rep)))
+    return CKPT_SOURCES[src.value], idx.value, rep.value
 
 
 def gdn_noalloc_scratch_bytes() -> int:

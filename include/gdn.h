@@ -212,6 +212,48 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
 size_t gdn_noalloc_scratch_bytes(void);
 
 /* ------------------------------------------------------------------------
+ * Chunked prefill with state checkpoints ("llama-memory: enable
+ * checkpointing with partial rollback", koboldcpp commits page, tag
+ * v1.113.1): the slots keep only the last n_slots states of a call, so a
+ * caller that may later keep fewer tokens (a shared prompt prefix, a
+ * rejected continuation) also wants states at regular positions. Computes
+ * exactly what gdn_forward_chunked computes and in addition stores
+ *   checkpoints[s][m] = state after token (m+1)*ckpt_every - 1 of sequence s
+ * (0-based within the sequence) for every m < max_ckpts with
+ * (m+1)*ckpt_every <= L_s. Entries a sequence does not reach are not
+ * written.
+ * checkpoints  device fp32 [N][max_ckpts][H][D_k][D_v], 16-byte aligned;
+ *              must not overlap state_in, state_slots or out
+ * ckpt_every   positive multiple of 64 (a chunk boundary)
+ * max_ckpts    >= 1
+ * The other arguments are those of gdn_forward_chunked.
+ * ---------------------------------------------------------------------- */
+gdn_status gdn_forward_chunked_checkpointed(
+    const gdn_varlen_shape *shape, const int32_t *cu_seqlens, const void *q, const void *k,
+    const void *v, const float *g, const float *beta, const float *const *state_in,
+    float *state_slots, float *out, int n_slots, gdn_mode mode, float *checkpoints,
+    int ckpt_every, int max_ckpts, void *workspace, size_t workspace_bytes,
+    gdn_stream_t stream);
+
+/*
+ * Where to restart a sequence of L tokens, last run with n_slots slots and
+ * checkpoints every ckpt_every tokens (max_ckpts of them), that keeps only
+ * its first n_keep tokens (0 <= n_keep <= L):
+ *   *source = 0: start from that call's state_in and replay tokens
+ *                [0, n_keep) (*index = -1, *replay_from = 0);
+ *   *source = 1: start from checkpoint *index and replay tokens
+ *                [*replay_from, n_keep);
+ *   *source = 2: the state is slot *index, nothing to replay
+ *                (*replay_from = n_keep).
+ * A slot is chosen whenever one holds the state; otherwise the latest
+ * checkpoint at or before n_keep. GDN_ERR_INVALID_ARG for bad arguments.
+ * Host only.
+ */
+gdn_status gdn_checkpoint_select(int n_keep, int L, int n_slots, int ckpt_every,
+                                 int max_ckpts, int *source, int *index,
+                                 int *replay_from);
+
+/* ------------------------------------------------------------------------
  * Rollback bookkeeping: a host-side table with one entry per sequence (the
  * recurrent memory's per-sequence record of which stored state is live,
  * "llama-memory-recurrent: clear rs_idx in clear", koboldcpp commits, tag
