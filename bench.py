@@ -225,6 +225,9 @@ class Decode:
                       f"{self.SETS - 1} steps earlier), {self.POOL} distinct token steps",
                 "timing": "CUDA graphs of consecutive steps, CUDA events on the launch stream"}
 
+    def launches_per_step(self):
+        return 1   # recurrent_kernel
+
     def alg_bytes_per_step(self):
         D = self.D
         per = 8 * D * D + (2 * D + D) * 2 + 4 + 4 + 4 * D   # 132,360 B per token-head
@@ -425,6 +428,11 @@ class Prefill:
 
     in_bytes = 2    # q, k, v element size
 
+    def launches_per_step(self):
+        if self.in_bytes == 4:
+            return 2   # work list, recurrent kernel (token-loop route)
+        return 4       # work list, chunk prep, chunk scan, recurrent tail
+
     def alg_bytes_per_step(self):
         g_bytes = 4 * 128 if self.mode == "kda" else 4
         per_tok_head = 3 * 128 * self.in_bytes + g_bytes + 4 + 4 * 128
@@ -577,11 +585,41 @@ class DecodeGQA(Decode):
             state["i"] += 1
             return n_seqs
         return run
+class PrefillVarlenCkpt(PrefillVarlen):
+    """The varlen batch through gdn_forward_chunked_checkpointed, with a
+    checkpoint every 1024 tokens of each sequence (up to 8 per sequence)."""
+    name = "prefill_varlen_ckpt"
+    EVERY, MAX_CKPTS = 1024, 8
+
+    def setup(self, gdn, dev):
+        super().setup(gdn, dev)
+        self.ckpts = torch.empty(self.N, self.MAX_CKPTS, self.H, 128, 128, device=dev)
+
+    def n_ckpts(self):
+        return int(sum(min(int(L) // self.EVERY, self.MAX_CKPTS) for L in self.b0.seq_len))
+
+    def alg_bytes_per_step(self):
+        return super().alg_bytes_per_step() + self.n_ckpts() * self.H * 128 * 128 * 4
+
+    def _call(self, d, q, k, v, g, beta, stream):
+        self.gdn.gdn_forward_chunked_checkpointed(
+            self.shape, d["cu"], q, k, v, g, beta, d["ptrs"], self.slots, self.out, self.K,
+            self.mode, self.ckpts, self.EVERY, self.MAX_CKPTS, self.ws, self.ws_bytes, stream)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("varlen GDA chunked prefill with state checkpoints every 1024 tokens "
+                         "(gdn_forward_chunked_checkpointed, up to 8 per sequence): "
+                         "8 sequences, lengths ~U[512,8192] (seed 4), H=16, D_k=D_v=128, "
+                         "bf16 q/k/v, fp32 state, K=8 slots")
+        c["checkpoints_per_step"] = sum(min(int(L) // self.EVERY, self.MAX_CKPTS)
+                                        for L in inputs.varlen_lengths(4))
+        return c
 
 
 WORKLOADS = {"decode": Decode, "verify": Verify, "prefill_kda": PrefillKDA,
              "decode_gqa": DecodeGQA, "prefill_varlen_fp32": PrefillVarlenF32,
-             "prefill_varlen": PrefillVarlen}
+             "prefill_varlen": PrefillVarlen, "prefill_varlen_ckpt": PrefillVarlenCkpt}
 
 
 # ----------------------------------------------------------------- arms
@@ -787,7 +825,7 @@ def gdn_arm(args, wl_cls):
                                  "peak_source": f"{src} hbm_gbs"},
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-            "gpu_launches": K * (4 if isinstance(wl, Prefill) else 1),
+            "gpu_launches": K * wl.launches_per_step(),
             **({"l2_warm_in_place": in_place} if in_place else {}),
             "clocks": summarize_clocks(clock_rows, t_wall0, t_wall1),
         }

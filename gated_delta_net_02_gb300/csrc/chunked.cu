@@ -661,6 +661,42 @@ __device__ __forceinline__ void named_bar(int id) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "n"(STATE_THREADS) : "memory");
 }
 
+// In-place 8 x 8 transpose of 16-byte pieces inside each group of 8 lanes:
+// lane 8g + a holding piece b of row 8g + a (x[4b .. 4b+3]) ends up holding
+// piece a of row 8g + b. Three xor-shuffle steps; applying it twice restores x.
+__device__ __forceinline__ void transpose8x8(float (&x)[32], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (b & m) continue;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float snd = hi ? x[4 * b + c] : x[4 * (b | m) + c];
+        const float rcv = __shfl_xor_sync(0xffffffffu, snd, m);
+        if (hi) x[4 * b + c] = rcv;
+        else x[4 * (b | m) + c] = rcv;
+      }
+    }
+  }
+}
+
+// Stores the 32 x 32 fp32 block a warp holds (lane l: row l, 32 consecutive
+// floats) to rows `ld` floats apart starting at dst: after transpose8x8 each
+// store instruction writes four whole 128-byte rows instead of 32 scattered
+// 16-byte pieces; a second transpose gives x back. Every lane must call it.
+__device__ __forceinline__ void store_rows32(float (&x)[32], float *dst, long long ld,
+                                             int lane) {
+  transpose8x8(x, lane);
+  const int g = lane >> 3, p = lane & 7;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4 *>(dst + (long long)(8 * g + u) * ld + 4 * p) =
+        make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+  transpose8x8(x, lane);
+}
+
 // Bounded wait that also gives up early once another role has aborted. On
 // a timeout the error word records the site (bits 8..15) and chunk (16..).
 __device__ __forceinline__ bool wait_ab(uint64_t *bar, uint32_t parity,
@@ -698,7 +734,9 @@ struct RoleSync {
   }
 };
 
-template <bool KDA>
+// CKPT: also store the checkpoints (a separate instance, so that the plain
+// prefill's chunk loop carries no trace of them)
+template <bool KDA, bool CKPT>
 __global__ void __launch_bounds__(SCAN_THREADS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_q,
@@ -821,22 +859,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       }
       ++issued;
       if (len < CH) {
-        // Only the last chunk can be partial. Its padding rows of V (and of
-        // the raw K and Q for GDA) hold the next tokens: zero them.
+        // Only the last chunk can be partial. Its padding rows hold the next
+        // tokens, whose values must not reach this chunk's results even as
+        // 0 * inf: zero those of V (rows of T V) and, for GDA, of the raw K
+        // (rows of K^T D~). Padding rows of Q only reach outputs that are
+        // not stored; KDA's K~ and Q^ come from the workspace, already padded.
         int ok = 1;
         if (lane == 0) ok = wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, 42, jc);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        constexpr int per_row = KDA ? 8 : 40;  // 16-byte pieces per padding row
+        constexpr int per_row = KDA ? 8 : 24;  // 16-byte pieces per padding row
         for (int e = lane; e < (CH - len) * per_row; e += 32) {
           const int r = len + e / per_row, c = e % per_row;
           unsigned char *dst;
-          if (c < 8) {
+          if (c < 8)
             dst = base + ST_V + r * 128 + c * 16;
-          } else if (c < 24) {
+          else
             dst = base + ST_K + ((c - 8) >> 3) * 8192 + r * 128 + ((c - 8) & 7) * 16;
-          } else {
-            dst = base + ST_WQ + ((c - 24) >> 3) * 16384 + (CH + r) * 128 + ((c - 24) & 7) * 16;
-          }
           *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
@@ -1077,16 +1115,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       if (tid == 0 && jc + 1 < nch) mbar_arrive(bE4);
       // checkpoint: the state after a full chunk that ends on a multiple of
       // ckpt_every tokens (chunks start at multiples of 64 in the sequence)
-      if (ckpt && w.chunk_len[chunk0 + jc] == CH) {
+      if (CKPT && w.chunk_len[chunk0 + jc] == CH) {
         const int pos = (jc + 1) * CH, c = pos / ckpt_every - 1;
-        if (pos % ckpt_every == 0 && c < max_ckpts) {
-          float4 *dst = reinterpret_cast<float4 *>(
-              ckpt + ((((long long)s * max_ckpts + c) * H + h) * DK + i) * DV + NV * vs +
-              32 * ch);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
-        }
+        if (pos % ckpt_every == 0 && c < max_ckpts)
+          store_rows32(Sm,
+                       ckpt + ((((long long)s * max_ckpts + c) * H + h) * DK + 32 * (warp & 3)) *
+                                  DV + NV * vs + 32 * ch,
+                       DV, lane);
       }
       // this chunk's outputs, while the next chunk's X is computed (the
       // staging tile is free once thread 0's earlier stores have read it)
@@ -1191,8 +1226,10 @@ cudaError_t set_attributes() {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
     if (e != cudaSuccess) return e;
   }
-  const void *sfns[] = {(const void *)chunk_scan_kernel<false>,
-                        (const void *)chunk_scan_kernel<true>};
+  const void *sfns[] = {(const void *)chunk_scan_kernel<false, false>,
+                        (const void *)chunk_scan_kernel<true, false>,
+                        (const void *)chunk_scan_kernel<false, true>,
+                        (const void *)chunk_scan_kernel<true, true>};
   for (const void *f : sfns) {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
     if (e != cudaSuccess) return e;
@@ -1275,14 +1312,23 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
           mq, mk, a.g, a.beta, a.H, Hqk, a.qk_grouped ? 1 : 0, w, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
-    if (a.kda)
-      chunk_scan_kernel<true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
-          a.scale, w, a.ckpt, a.ckpt_every, a.max_ckpts, a.err);
+    const int qg = a.qk_grouped ? 1 : 0;
+    if (a.kda && a.ckpt)
+      chunk_scan_kernel<true, true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
+          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+          a.ckpt_every, a.max_ckpts, a.err);
+    else if (a.kda)
+      chunk_scan_kernel<true, false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
+          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr,
+          1, 0, a.err);
+    else if (a.ckpt)
+      chunk_scan_kernel<false, true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
+          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+          a.ckpt_every, a.max_ckpts, a.err);
     else
-      chunk_scan_kernel<false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, a.qk_grouped ? 1 : 0,
-          a.scale, w, a.ckpt, a.ckpt_every, a.max_ckpts, a.err);
+      chunk_scan_kernel<false, false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
+          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr, 1,
+          0, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 

@@ -107,6 +107,15 @@ def test_checkpoints_match_oracle_bf16(gdn, mode, every, max_ckpts):
     assert torch.equal(slots.nan_to_num(7.0), slots0.nan_to_num(7.0))
 
 
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+def test_checkpoints_with_a_long_tail(gdn, mode):
+    # 70 slots: the last 70 tokens go through the recurrent kernel, which
+    # writes the boundaries among them (L=257: 192 and 256; L=320: 256, 320)
+    b = inputs.make_batch(76, [700, 257, 320, 30], 2, 128, 128, mode=mode, n_slots=70)
+    _, _, cks = run(gdn, b, 64, 12)
+    assert check_checkpoints(b, cks, 64, 12, TOL[torch.bfloat16]) == 10 + 4 + 5
+
+
 @pytest.mark.parametrize("dtype,D", [(torch.float32, 128), (torch.bfloat16, 64)])
 def test_checkpoints_token_loop_route(gdn, dtype, D):
     b = inputs.make_batch(72, [300, 130, 64, 5], 2, D, D, mode="gda", n_slots=3, dtype=dtype)

@@ -101,6 +101,18 @@ def test_varlen_prefill_full_size(gdn):
     print(f"varlen prefill: out rel-L2 {e_out:.2e}, state rel-L2 {e_fin:.2e}")
 
 
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("n_slots", [1, 64, 65])
+def test_slot_counts_around_one_chunk(gdn, mode, n_slots):
+    # the recurrent tail covers the last n_slots tokens: a whole chunk's
+    # worth and more; lengths below, at and above n_slots, so the chunked
+    # part ends on and off chunk boundaries
+    lens = [300, 64, 130, 40, 65, 1]
+    b = inputs.make_batch(47, lens, 2, 128, 128, mode=mode, n_slots=n_slots)
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)
+
+
 def test_matches_recurrent_path(gdn):
     b = inputs.make_batch(43, [300, 300], 2, 128, 128, mode="gda", n_slots=2)
     out_c, sl_c = chunked_forward(gdn, b)
