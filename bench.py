@@ -206,6 +206,7 @@ class Decode:
     double-buffered state; step i advances batch i % SETS, so between two
     steps of one batch the other batches move (SETS-1) x 128 MiB through
     the memory system and its state is read from HBM, not L2."""
+    compute_dtype = "f32"   # fp32 state arithmetic on CUDA cores (bf16 inputs widened)
     N, H, D = 64, 16, 128
     POOL = 256      # distinct token steps resident on the device
     SETS = 8        # independent batches (8 x 2 x 64 MiB = 1 GiB)
@@ -427,6 +428,8 @@ class Prefill:
         return self.ntok
 
     in_bytes = 2    # q, k, v element size
+    # tensor-core products of bf16 operands, fp32 accumulation and state
+    compute_dtype = "bf16"
 
     def launches_per_step(self):
         if self.in_bytes == 4:
@@ -521,6 +524,7 @@ class PrefillVarlenF32(PrefillVarlen):
     loop (the recurrent kernel) for every token."""
     name = "prefill_varlen_fp32"
     in_bytes = 4
+    compute_dtype = "f32"   # token loop on CUDA cores
 
     def batch(self, j):
         lens = inputs.varlen_lengths(4)
@@ -817,7 +821,7 @@ def gdn_arm(args, wl_cls):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": ms_max / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic", "config": wl.config(),
+            "dtype": wl.compute_dtype, "data": "synthetic", "config": wl.config(),
             "roofline": roof or {"bound": "hbm", "achieved": achieved, "peak": hbm,
                                  "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                                  "kernel": "recurrent_kernel (gdn_forward)",
