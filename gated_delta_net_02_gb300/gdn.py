@@ -103,10 +103,15 @@ lib.gdn_check_device_error.argtypes = [_vp]
 
 
 def _addr(x):
+    """Device address of a tensor argument (or a raw integer address). The C
+    ABI takes packed row-major buffers, so a strided view is refused here
+    rather than read as if it were packed."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError("gdn: tensor arguments must be contiguous (packed row-major)")
     return x.data_ptr()
 
 

@@ -186,3 +186,13 @@ def test_grouped_query_heads_are_validated_on_the_host(gdn):
     assert call_forward(gdn, shape(gdn, H=4, H_qk=2, qk_map=gdn.GDN_QK_GROUPED), q=0) \
         == gdn.GDN_ERR_INVALID_ARG
     assert "q is NULL" in gdn.gdn_last_error()
+
+
+def test_binding_refuses_strided_views(gdn):
+    # the C ABI has no strides: a transposed view must not reach it
+    import torch
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        gdn._addr(x.t())
+    assert gdn._addr(x) == x.data_ptr()
+    assert gdn._addr(None) is None and gdn._addr(1 << 20) == 1 << 20
