@@ -146,6 +146,7 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
   a.bf16 = s.in_dtype == GDN_BF16;
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
   a.err = err;
+  a.pdl = true;  // prologue overlaps the previous kernel of the stream
   return check_launch(gdn::launch_recurrent(a, reinterpret_cast<cudaStream_t>(stream)),
                       "gdn_forward launch");
 }

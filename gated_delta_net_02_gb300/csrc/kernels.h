@@ -28,6 +28,9 @@ struct RecurrentArgs {
   float *ckpt = nullptr;        // [n_seqs][max_ckpts][H][Dk][Dv]
   const int *pos0 = nullptr;    // device [n_seqs] position of the first token (NULL = 0)
   int ckpt_every = 0, max_ckpts = 0;
+  // programmatic launch (gdn_forward only: tok_start and seq_len must be NULL,
+  // since the kernel reads its scalars before waiting for its predecessor)
+  bool pdl = false;
 };
 
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);

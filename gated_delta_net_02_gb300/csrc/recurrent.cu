@@ -42,6 +42,7 @@ struct RecParams {
   int n_seqs, T, H, n_slots;
   int Hqk, qk_grouped;  // q/k heads and the value-head -> q/k-head map
   float *ckpt;          // optional checkpoints, [n_seqs][max_ckpts][H][Dk][Dv]
+  int pdl;              // launched programmatically (tok_start, seq_len, ckpt NULL)
   const int *pos0;      // position of each sequence's first token (NULL = 0)
   int ckpt_every, max_ckpts;
   float scale;
@@ -140,6 +141,9 @@ __global__ void __launch_bounds__(C::NT)
   constexpr int DK = C::DK, DV = C::DV, ROWG = C::ROWG, CG = C::CG;
   constexpr int RPT = C::RPT, TT = C::TT, CCOLS = C::CCOLS;
 
+  // The next kernel of the stream (if launched programmatically) may be
+  // scheduled once every block of this one has started.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(128) unsigned char smem[];
   float *fq = reinterpret_cast<float *>(smem + 2 * C::RAW_BYTES);
   float *fk = fq + TT * DK;
@@ -215,6 +219,12 @@ __global__ void __launch_bounds__(C::NT)
     }
   };
 
+  // Launched programmatically (gdn_forward), this grid may have been scheduled
+  // while the previous kernel of the stream runs: nothing in global memory
+  // has been read or written up to here (T and the token offsets are launch
+  // parameters then), and nothing is before that kernel completes. Without
+  // a programmatic launch the wait returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // token copies and gate scalars first, then the state pointer
   if (warp == 0) issue(0, 0);
   float g_cur, b_cur;
@@ -346,6 +356,9 @@ cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   static_assert(C::SMEM <= 48 * 1024, "fits the default shared-memory window");
+  if (p.pdl)  // gdn_forward: overlaps the previous kernel's tail with this prologue
+    return launch_pdl(recurrent_kernel<C, false>, dim3((unsigned)n_items), dim3(C::NT), C::SMEM,
+                      stream, p);
   if (p.ckpt)
     recurrent_kernel<C, true><<<(unsigned)n_items, C::NT, C::SMEM, stream>>>(p);
   else
@@ -374,6 +387,7 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
   p.Hqk = a.Hqk > 0 ? a.Hqk : a.H;
   p.qk_grouped = a.qk_grouped ? 1 : 0;
   p.ckpt = a.ckpt; p.pos0 = a.pos0;
+  p.pdl = a.pdl && !a.tok_start && !a.seq_len && !a.ckpt ? 1 : 0;
   p.ckpt_every = a.ckpt_every > 0 ? a.ckpt_every : 1; p.max_ckpts = a.max_ckpts;
   p.scale = a.scale; p.err = a.err;
   if (a.Dk == 128 && a.Dv == 128) return launch_d<128, 128>(p, a.kda, a.bf16, stream);

@@ -115,6 +115,10 @@ typedef struct {
  * out         device fp32 [N*T][H][D_v]
  * n_slots     K >= 1
  * Returns GDN_OK once the kernel is enqueued on `stream`.
+ * The kernel is a programmatic dependent launch: its blocks may be scheduled
+ * while the previous kernel of `stream` is still running, but they read and
+ * write no memory until that kernel has completed, so stream order holds for
+ * every argument as for an ordinary launch.
  */
 gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
                        const void *v, const float *g, const float *beta,
