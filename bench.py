@@ -199,6 +199,35 @@ def capture(fn_steps, stream, steps):
 
 # ----------------------------------------------------------------- workloads
 
+class PackedInputs:
+    """End-to-end staging: a step's host inputs (q, k, v, g, beta) packed at
+    256-byte offsets in one pinned buffer per step, copied with one
+    host-to-device copy into a device buffer of the same layout, whose typed
+    views are what the API call receives."""
+
+    def __init__(self, host, dev):
+        # host: tensors with a leading step dimension [P, ...] (P may be 1)
+        P = host[0].shape[0]
+        self.offs, self.nbytes = [], []
+        off = 0
+        for t in host:
+            nb = t[0].numel() * t.element_size()
+            self.offs.append(off)
+            self.nbytes.append(nb)
+            off = (off + nb + 255) // 256 * 256
+        self.step_bytes = off
+        self.host = torch.zeros(P, off, dtype=torch.uint8).pin_memory()
+        for t, o, nb in zip(host, self.offs, self.nbytes):
+            self.host[:, o:o + nb].copy_(t.reshape(P, -1).view(torch.uint8))
+        self.stage = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.views = [self.stage[o:o + nb].view(t.dtype).view(t.shape[1:])
+                      for t, o, nb in zip(host, self.offs, self.nbytes)]
+
+    def copy_in(self, p):
+        self.stage.copy_(self.host[p], non_blocking=True)
+        return self.views
+
+
 class Decode:
     """64 sequences x 1 token, H=16, D=128, GDA, bf16 q/k/v, fp32 state.
 
@@ -247,11 +276,10 @@ class Decode:
         self.dev = [h.to(dev) for h in self.host]
         self.out = torch.empty(N, H, D, device=dev)
         self.shape = gdn.gdn_shape(N, 1, H, D, D, gdn.GDN_BF16, D ** -0.5)
-        # e2e: pinned host pool, device staging, pinned host output
-        self.pinned = [h.pin_memory() for h in self.host]
-        self.stage = [torch.empty_like(d[0]) for d in self.dev]
+        # e2e: packed pinned host pool, one device staging buffer, pinned output
+        self.packed = PackedInputs(self.host, dev)
         self.out_host = torch.empty(N, H, D, dtype=torch.float32).pin_memory()
-        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
     def _bufs(self, i):
@@ -269,11 +297,8 @@ class Decode:
                              stream)
 
     def step_e2e(self, i, stream):
-        p = i % self.POOL
-        for s, h in zip(self.stage, self.pinned):
-            s.copy_(h[p], non_blocking=True)
+        q, k, v, g, beta = self.packed.copy_in(i % self.POOL)
         src, dst = self._bufs(i)
-        q, k, v, g, beta = self.stage
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, self.out, 1, "gda",
                              stream)
         self.out_host.copy_(self.out, non_blocking=True)
@@ -351,10 +376,9 @@ class Verify(Decode):
         self.slots = torch.empty(N, K, H, D, D, device=dev)
         self.out = torch.empty(N * T, H, D, device=dev)
         self.shape = gdn.gdn_shape(N, T, H, D, D, gdn.GDN_BF16, D ** -0.5)
-        self.pinned = [h.pin_memory() for h in self.host]
-        self.stage = [torch.empty_like(d[0]) for d in self.dev]
+        self.packed = PackedInputs(self.host, dev)
         self.out_host = torch.empty(N * T, H, D, dtype=torch.float32).pin_memory()
-        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
     def step(self, i, stream):
@@ -364,10 +388,7 @@ class Verify(Decode):
                              self.slots, self.out, self.K, "gda", stream)
 
     def step_e2e(self, i, stream):
-        p = i % self.POOL
-        for s, h in zip(self.stage, self.pinned):
-            s.copy_(h[p], non_blocking=True)
-        q, k, v, g, beta = self.stage
+        q, k, v, g, beta = self.packed.copy_in(i % self.POOL)
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
                              self.slots, self.out, self.K, "gda", stream)
         self.out_host.copy_(self.out, non_blocking=True)
@@ -417,10 +438,10 @@ class Prefill:
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.slots = torch.empty(self.N, self.K, self.H, 128, 128, device=dev)
         self.out = torch.empty(self.ntok, self.H, 128, device=dev)
-        self.pinned = [getattr(b0, n).pin_memory() for n in ("q", "k", "v", "g", "beta")]
-        self.stage = [t.to(dev) for t in self.pinned]
+        self.packed = PackedInputs([getattr(b0, n).unsqueeze(0)
+                                    for n in ("q", "k", "v", "g", "beta")], dev)
         self.out_host = torch.empty(self.ntok, self.H, 128).pin_memory()
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.pinned)
+        self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
     @property
@@ -456,10 +477,8 @@ class Prefill:
         self._call(d, d["q"], d["k"], d["v"], d["g"], d["beta"], stream)
 
     def step_e2e(self, i, stream):
-        for st, h in zip(self.stage, self.pinned):
-            st.copy_(h, non_blocking=True)
+        q, k, v, g, beta = self.packed.copy_in(0)
         _, d = self.sets[0]
-        q, k, v, g, beta = self.stage
         self._call(d, q, k, v, g, beta, stream)
         self.out_host.copy_(self.out, non_blocking=True)
 
@@ -565,9 +584,8 @@ class DecodeGQA(Decode):
         for lst in (self.host, self.dev):
             for i in (0, 1):  # q, k keep their first H_qk heads
                 lst[i] = lst[i][:, :, :hq].contiguous()
-        self.pinned = [h.pin_memory() for h in self.host]
-        self.stage = [torch.empty_like(d[0]) for d in self.dev]
-        self.h2d_bytes = sum(t[0].numel() * t[0].element_size() for t in self.host)
+        self.packed = PackedInputs(self.host, dev)
+        self.h2d_bytes = self.packed.step_bytes
         self.shape = gdn.gdn_shape(self.N, 1, self.H, self.D, self.D, gdn.GDN_BF16,
                                    self.D ** -0.5, hq, gdn.GDN_QK_GROUPED)
 
