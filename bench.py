@@ -646,8 +646,9 @@ WORKLOADS = {"decode": Decode, "verify": Verify, "prefill_kda": PrefillKDA,
 
 # ----------------------------------------------------------------- arms
 
-def run_cpu_baseline(wl, budget_s=15.0):
-    """The oracle, as it stands, on this host's cores, on a bounded sample."""
+def run_cpu_baseline(wl, budget_s=10.0):
+    """The oracle, as it stands, on this host's cores, on a bounded sample
+    (about budget_s seconds of work on all cores, a third of that on one)."""
     import oracle
     cores = oracle.max_threads()
     n_seqs = wl.N
@@ -655,7 +656,7 @@ def run_cpu_baseline(wl, budget_s=15.0):
     t = time.perf_counter()
     fn()
     one = time.perf_counter() - t
-    reps = max(1, min(200, int(budget_s / max(one, 1e-6))))
+    reps = max(1, min(20000, int(budget_s / max(one, 1e-6))))
     tok = 0
     t = time.perf_counter()
     for _ in range(reps):
@@ -666,7 +667,7 @@ def run_cpu_baseline(wl, budget_s=15.0):
     t = time.perf_counter()
     fn1()
     one1 = time.perf_counter() - t
-    reps1 = max(1, min(50, int(budget_s / 3 / max(one1, 1e-6))))
+    reps1 = max(1, min(5000, int(budget_s / 3 / max(one1, 1e-6))))
     tok1 = 0
     t = time.perf_counter()
     for _ in range(reps1):
