@@ -190,3 +190,14 @@ def test_restart_from_selected_state(gdn, mode):
     ref = oracle_prefix_state(b, n_keep)
     e = rel_l2(got, ref)
     assert e <= TOL[torch.bfloat16], f"restarted state rel-L2 {e}"
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+@pytest.mark.parametrize("qk_map", ["tiled", "grouped"])
+def test_checkpoints_with_grouped_query_heads(gdn, mode, qk_map):
+    # 4 value heads reading 2 q/k heads; boundaries in the scan and (L=257)
+    # in the tail: 6 + 2 + 4 checkpoints reached
+    b = inputs.make_batch(77, [400, 130, 257], 4, 128, 128, mode=mode, n_slots=4, H_qk=2,
+                          qk_map=qk_map)
+    _, _, cks = run(gdn, b, 64, 8)
+    assert check_checkpoints(b, cks, 64, 8, TOL[torch.bfloat16]) == 6 + 2 + 4
