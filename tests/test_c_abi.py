@@ -1,0 +1,32 @@
+"""The boundary from C (no GPU): tests/c_abi/host_abi.c is compiled as C11
+with warnings as errors against include/gdn.h, linked to the in-tree
+libgdn.so and run; it exercises the host-side calls and returns 0 when every
+check holds."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib_dir():
+    from gated_delta_net_02_gb300 import build
+    return os.path.dirname(build.build())
+
+
+def test_header_compiles_as_c_and_host_calls_work(lib_dir, tmp_path):
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "host_abi")
+    cmd = [cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c_abi", "host_abi.c"), "-o", exe, "-L", lib_dir,
+           "-lgdn", f"-Wl,-rpath,{lib_dir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "passed" in r.stdout
