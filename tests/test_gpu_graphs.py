@@ -73,3 +73,43 @@ def test_chunked_prefill_in_a_graph(gdn, mode):
     gdn.gdn_check_device_error()
     assert torch.equal(out, eager_out)
     assert torch.equal(slots.nan_to_num(0.0), eager_slots.nan_to_num(0.0))
+
+
+def test_checkpointed_prefill_in_a_graph(gdn):
+    # the checkpoint instance of the scan kernel and the tail's checkpoint
+    # stores, captured and replayed, equal an eager call bit for bit
+    b = inputs.make_batch(252, [300, 140, 5], 2, 128, 128, mode="gda", n_slots=3)
+    d = to_dev(b)
+    N, ntok, H = 3, b.q.shape[0], 2
+    cu = b.cu_seqlens.to(torch.int32).cuda()
+    shape = gdn.gdn_varlen_shape(N, ntok, H, 128, 128, gdn.GDN_BF16, b.scale)
+    ws_bytes = gdn.gdn_chunked_workspace_size(shape, 3)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ptrs = gdn.state_ptr_array(gdn.per_seq_state_ptrs(d["state"], N), "cuda")
+
+    def run(out, slots, cks, stream=None):
+        gdn.gdn_forward_chunked_checkpointed(shape, cu, d["q"], d["k"], d["v"], d["g"],
+                                             d["beta"], ptrs, slots, out, 3, "gda", cks, 64, 4,
+                                             ws, ws_bytes, stream)
+
+    def bufs():
+        return (torch.full((ntok, H, 128), float("nan"), device="cuda"),
+                torch.full((N, 3, H, 128, 128), float("nan"), device="cuda"),
+                torch.full((N, 4, H, 128, 128), float("nan"), device="cuda"))
+
+    eager = bufs()
+    run(*eager)
+    torch.cuda.synchronize()
+    got = bufs()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        run(*got, s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_error()
+    for x, y in zip(got, eager):
+        assert torch.equal(x.nan_to_num(0.0), y.nan_to_num(0.0))
+    assert not torch.isnan(got[2][0]).any()  # L=300 reaches all 4 checkpoints
