@@ -1,16 +1,19 @@
 """Benchmark of the GDN hot path on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
-                    [--workload decode|verify|prefill_kda|prefill_varlen]
+                    [--workload all|decode|verify|prefill_kda|prefill_varlen|...]
 
-Default workload (the headline): batched decode, 64 sequences x 1 token,
-H=16, D_k=D_v=128, GDA gate, bf16 q/k/v, fp32 state ~N(0, 0.05); one step is
-one decode step (64 tokens) through gdn_forward. Prints ONE JSON line on rank
-0. Inputs are resident in HBM when the timed region starts; the state chain
-rotates over enough banks that the working set is several times the L2, so
-every step reads its state from HBM. The "e2e" figure repeats the measurement
-with each step's tokens copied from pinned host memory and the outputs copied
-back, inside the timed region.
+Headline workload: batched decode, 64 sequences x 1 token, H=16,
+D_k=D_v=128, GDA gate, bf16 q/k/v, fp32 state ~N(0, 0.05); one step is one
+decode step (64 tokens) through gdn_forward. The default run (--workload
+all) then measures speculative verify, the KDA chunked prefill and the varlen
+GDA chunked prefill the same way (K timed steps after W warm-up steps each),
+and reports them under "workloads" in the same JSON line. Prints ONE JSON
+line on rank 0. Inputs are resident in HBM when the timed region starts; the
+inputs of every workload are larger than the L2 (decode rotates over enough
+state banks that every step reads its state from HBM). The "e2e" figure
+repeats the measurement with each step's inputs copied from pinned host
+memory and the outputs copied back, inside the timed region.
 
 --impl reference times the fp64 CPU oracle (a deliberately slow baseline) on
 the same workload, on this host's cores, on a bounded sample per step.
@@ -639,6 +642,9 @@ class PrefillVarlenCkpt(PrefillVarlen):
         return c
 
 
+# the default run: the headline first, then the other workloads of the metric
+ALL_WORKLOADS = ["decode", "verify", "prefill_kda", "prefill_varlen"]
+
 WORKLOADS = {"decode": Decode, "verify": Verify, "prefill_kda": PrefillKDA,
              "decode_gqa": DecodeGQA, "prefill_varlen_fp32": PrefillVarlenF32,
              "prefill_varlen": PrefillVarlen, "prefill_varlen_ckpt": PrefillVarlenCkpt}
@@ -717,22 +723,10 @@ def reference_arm(args, wl_cls):
     return 0
 
 
-def gdn_arm(args, wl_cls):
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from gated_delta_net_02_gb300 import build
-    build.build()
-    from gated_delta_net_02_gb300 import gdn
-
-    wl = wl_cls()
-    wl.setup(gdn, dev)
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize()
-
+def measure(wl, args, gdn, dev, stream, ws, rank, local):
+    """Times K steps of workload `wl` (CUDA graphs of consecutive steps,
+    events on the launch stream), then K end-to-end steps; returns this
+    rank's figures and the clock record of the timed region."""
     def barrier():
         if ws > 1:
             import torch.distributed as dist
@@ -773,6 +767,7 @@ def gdn_arm(args, wl_cls):
     time.sleep(0.15)
     clock_rows = sampler.stop() if sampler else []
     gdn.gdn_check_device_error(stream)
+    del graphs
 
     # e2e: host tokens in, host outputs back, per step, same K
     graphs_e2e = graphs_for(wl.step_e2e)
@@ -784,6 +779,7 @@ def gdn_arm(args, wl_cls):
     ms_e2e = timed_graph_steps(graphs_e2e, K, stream)
     barrier()
     gdn.gdn_check_device_error(stream)
+    del graphs_e2e
 
     in_place = None
     if wl.name == "decode" and K >= L:
@@ -802,59 +798,98 @@ def gdn_arm(args, wl_cls):
                     "note": "one 64-sequence batch stepping in place: its 64 MiB state "
                             "ping-pongs between two buffers and largely stays in L2; an L2 "
                             "figure beside the cold-L2 headline, not the headline"}
+    return ms, ms_e2e, in_place, summarize_clocks(clock_rows, t_wall0, t_wall1)
 
-    ms_max, ms_e2e_max, value, e2e_value = aggregate_over_ranks(
-        ms, ms_e2e, wl.tokens_per_step, K, ws, dev)
 
+def roofline(wl, kern_s):
+    """Roofline object of one workload from its average step duration."""
+    peaks, src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = wl.alg_bytes_per_step() / kern_s / 1e9
+    if isinstance(wl, Prefill):
+        sha = source_sha("chunked.cu", "recurrent.cu", "umma.cuh", "common.cuh")
+        tflops = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        flops = wl.alg_flops_per_step() / kern_s / 1e12
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm,
+                "traffic": ncu_traffic("gdn_chunked_" + wl.name, sha),
+                "kernel": "whole gdn_forward_chunked call (work list, chunk prep, "
+                          "chunk scan, recurrent tail)",
+                "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
+                "tensor": {"achieved": flops, "peak": tflops, "unit": "TFLOP/s",
+                           "frac": flops / tflops,
+                           "algorithmic_flops_per_launch": wl.alg_flops_per_step()},
+                # ideal time of the binding roofline / measured time
+                "binding_frac": max(achieved / hbm, flops / tflops),
+                "peak_source": f"{src} hbm_gbs and bf16_tflops (burst)"}
+        if wl.in_bytes == 4:  # token-loop route: fp32 CUDA-core work, HBM-bound
+            roof["tensor"] = None
+            roof["binding_frac"] = achieved / hbm
+            roof["kernel"] = "whole gdn_forward_chunked call (token-loop route: work list, " \
+                             "recurrent kernel)"
+        return roof
+    sha = source_sha("recurrent.cu", "common.cuh")
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": ncu_traffic("gdn_recurrent_" + wl.name, sha),
+            "kernel": "recurrent_kernel (gdn_forward)",
+            "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
+            "peak_source": f"{src} hbm_gbs"}
+
+
+def gdn_arm(args, names):
+    """Measures the workloads `names` in order; the first is the headline
+    (top-level keys of the JSON line), the others go under "workloads"."""
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from gated_delta_net_02_gb300 import build
+    build.build()
+    from gated_delta_net_02_gb300 import gdn
+
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+    lines = []
+    for name in names:
+        wl = WORKLOADS[name]()
+        wl.setup(gdn, dev)
+        torch.cuda.synchronize()
+        ms, ms_e2e, in_place, clocks = measure(wl, args, gdn, dev, stream, ws, rank, local)
+        ms_max, ms_e2e_max, value, e2e_value = aggregate_over_ranks(
+            ms, ms_e2e, wl.tokens_per_step, K, ws, dev)
+        line = None
+        if rank == 0:
+            kern_s = ms / K / 1e3  # this rank's average launch duration
+            line = {
+                "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+                "steps": K, "warmup": W, "ms_per_step": ms_max / K,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": wl.compute_dtype, "data": "synthetic", "config": wl.config(),
+                "roofline": roofline(wl, kern_s),
+                "e2e": {"value": e2e_value, "unit": "tokens/s",
+                        "h2d_bytes_per_step": wl.h2d_bytes,
+                        "d2h_bytes_per_step": wl.d2h_bytes},
+                "gpu_launches": K * wl.launches_per_step(),
+                **({"l2_warm_in_place": in_place} if in_place else {}),
+                "clocks": clocks,
+            }
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = run_cpu_baseline(wl)
+        lines.append(line)
+        del wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     if rank == 0:
-        peaks, src = measured_peaks()
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-        kern_s = ms / K / 1e3  # this rank's average launch duration
-        achieved = wl.alg_bytes_per_step() / kern_s / 1e9
-        if isinstance(wl, Prefill):
-            sha = source_sha("chunked.cu", "recurrent.cu", "umma.cuh", "common.cuh")
-            tflops = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-            flops = wl.alg_flops_per_step() / kern_s / 1e12
-            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm,
-                    "traffic": ncu_traffic("gdn_chunked_" + wl.name, sha),
-                    "kernel": "whole gdn_forward_chunked call (work list, chunk prep, "
-                              "chunk scan, recurrent tail)",
-                    "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
-                    "tensor": {"achieved": flops, "peak": tflops, "unit": "TFLOP/s",
-                               "frac": flops / tflops,
-                               "algorithmic_flops_per_launch": wl.alg_flops_per_step()},
-                    # ideal time of the binding roofline / measured time
-                    "binding_frac": max(achieved / hbm, flops / tflops),
-                    "peak_source": f"{src} hbm_gbs and bf16_tflops"}
-            if wl.in_bytes == 4:  # token-loop route: fp32 CUDA-core work, HBM-bound
-                roof["tensor"] = None
-                roof["binding_frac"] = achieved / hbm
-                roof["kernel"] = "whole gdn_forward_chunked call (token-loop route: work list, " \
-                                 "recurrent kernel)"
-        else:
-            sha = source_sha("recurrent.cu", "common.cuh")
-            roof = None
-        traffic = ncu_traffic("gdn_recurrent_" + wl.name, sha)
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-            "steps": K, "warmup": W, "ms_per_step": ms_max / K,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": wl.compute_dtype, "data": "synthetic", "config": wl.config(),
-            "roofline": roof or {"bound": "hbm", "achieved": achieved, "peak": hbm,
-                                 "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                                 "kernel": "recurrent_kernel (gdn_forward)",
-                                 "algorithmic_bytes_per_launch": wl.alg_bytes_per_step(),
-                                 "peak_source": f"{src} hbm_gbs"},
-            "e2e": {"value": e2e_value, "unit": "tokens/s",
-                    "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-            "gpu_launches": K * wl.launches_per_step(),
-            **({"l2_warm_in_place": in_place} if in_place else {}),
-            "clocks": summarize_clocks(clock_rows, t_wall0, t_wall1),
-        }
-        if not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_cpu_baseline(wl)
-        print(json.dumps(line), flush=True)
+        head = lines[0]
+        if len(lines) > 1:
+            head["gpu_launches_all_workloads"] = sum(x["gpu_launches"] for x in lines)
+            head["workloads"] = {n: {k: v for k, v in x.items()
+                                     if k not in ("metric", "n_gpus", "higher_is_better",
+                                                  "scaling", "vs_baseline", "data")}
+                                 for n, x in zip(names[1:], lines[1:])}
+        print(json.dumps(head), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -862,21 +897,59 @@ def gdn_arm(args, wl_cls):
     return 0
 
 
+def ncu_range(args, name):
+    """W eager warm-up steps, then `--ncu-range N` eager steps between
+    cudaProfilerStart/Stop, for an ncu range-replay capture of the DRAM bytes
+    of N consecutive steps (the write-back of one step's state counts even
+    when it leaves L2 during the next). Prints the step count only."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from gated_delta_net_02_gb300 import build
+    build.build()
+    from gated_delta_net_02_gb300 import gdn
+    wl = WORKLOADS[name]()
+    wl.setup(gdn, dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            wl.step(i, stream)
+    stream.synchronize()
+    gdn.gdn_check_device_error(stream)
+    n = args.ncu_range
+    torch.cuda.profiler.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup, args.warmup + n):
+            wl.step(i, stream)
+    stream.synchronize()
+    torch.cuda.profiler.stop()
+    gdn.gdn_check_device_error(stream)
+    print(json.dumps({"ncu_range": name, "steps_in_range": n,
+                      "launches_per_step": wl.launches_per_step()}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20480)
-    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=["all"] + sorted(WORKLOADS), default="all",
+                    help="all (default): decode as the headline, then verify, KDA prefill "
+                         "and varlen prefill under 'workloads'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-range", type=int, default=0,
+                    help="profiling aid: run N eager steps between cudaProfilerStart/Stop "
+                         "(for ncu --replay-mode range) and print no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    wl_cls = WORKLOADS[args.workload]
+    names = ALL_WORKLOADS if args.workload == "all" else [args.workload]
+    if args.ncu_range:
+        return ncu_range(args, names[0])
     if args.impl == "reference":
-        return reference_arm(args, wl_cls)
-    return gdn_arm(args, wl_cls)
+        return reference_arm(args, WORKLOADS[names[0]])
+    return gdn_arm(args, names)
 
 
 if __name__ == "__main__":

@@ -159,15 +159,13 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots) {
                                      shape->D_k, shape->D_v, shape->in_dtype == GDN_BF16);
 }
 
-// Validation and launch shared by gdn_forward_chunked (ckpt = NULL) and
-// gdn_forward_chunked_checkpointed.
-static gdn_status chunked_call(const char *fn, const gdn_varlen_shape *shape,
+// Argument checks shared by every chunked entry point, and the launch
+// arguments they imply (all but the workspace and the checkpoints).
+static gdn_status chunked_args(const char *fn, const gdn_varlen_shape *shape,
                                const int32_t *cu_seqlens, const void *q, const void *k,
                                const void *v, const float *g, const float *beta,
                                const float *const *state_in, float *state_slots, float *out,
-                               int n_slots, gdn_mode mode, float *ckpt, int ckpt_every,
-                               int max_ckpts, void *workspace, size_t workspace_bytes,
-                               gdn_stream_t stream) {
+                               int n_slots, gdn_mode mode, gdn::ChunkedArgs *a) {
   if (!shape) return fail(GDN_ERR_INVALID_ARG, "%s: shape is NULL", fn);
   const gdn_varlen_shape &s = *shape;
   if (s.n_seqs <= 0 || s.total_tokens < 0 || s.H <= 0)
@@ -190,9 +188,9 @@ static gdn_status chunked_call(const char *fn, const gdn_varlen_shape *shape,
     return GDN_ERR_INVALID_ARG;
   if ((long long)s.total_tokens * s.H > (1LL << 31))
     return fail(GDN_ERR_UNSUPPORTED, "%s: too many token-heads", fn);
-  const void *ptrs[] = {cu_seqlens, state_in, state_slots, workspace};
-  const char *names[] = {"cu_seqlens", "state_in", "state_slots", "workspace"};
-  for (int i = 0; i < 4; ++i)
+  const void *ptrs[] = {cu_seqlens, state_in, state_slots};
+  const char *names[] = {"cu_seqlens", "state_in", "state_slots"};
+  for (int i = 0; i < 3; ++i)
     if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
   if (s.total_tokens > 0) {
     const void *tp[] = {q, k, v, g, beta, out};
@@ -205,29 +203,43 @@ static gdn_status chunked_call(const char *fn, const gdn_varlen_shape *shape,
   }
   if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
     return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
+
+  *a = gdn::ChunkedArgs{};
+  a->cu_seqlens = cu_seqlens;
+  a->q = q; a->k = k; a->v = v; a->g = g; a->beta = beta;
+  a->state_in = state_in; a->slots = state_slots; a->out = out;
+  a->n_seqs = s.n_seqs; a->total_tokens = s.total_tokens; a->H = s.H;
+  a->Hqk = hq; a->qk_grouped = s.qk_map == GDN_QK_GROUPED;
+  a->bf16 = s.in_dtype == GDN_BF16;
+  a->Dk = s.D_k; a->Dv = s.D_v; a->n_slots = n_slots;
+  a->kda = mode == GDN_MODE_KDA;
+  a->scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
+  return GDN_OK;
+}
+
+// Validation and launch shared by gdn_forward_chunked (ckpt = NULL) and
+// gdn_forward_chunked_checkpointed.
+static gdn_status chunked_call(const char *fn, const gdn_varlen_shape *shape,
+                               const int32_t *cu_seqlens, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const float *const *state_in, float *state_slots, float *out,
+                               int n_slots, gdn_mode mode, float *ckpt, int ckpt_every,
+                               int max_ckpts, void *workspace, size_t workspace_bytes,
+                               gdn_stream_t stream) {
+  gdn::ChunkedArgs a;
+  gdn_status st = chunked_args(fn, shape, cu_seqlens, q, k, v, g, beta, state_in, state_slots,
+                               out, n_slots, mode, &a);
+  if (st != GDN_OK) return st;
+  if (!workspace) return fail(GDN_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(GDN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
   const size_t need = gdn_chunked_workspace_size(shape, n_slots);
   if (workspace_bytes < need)
     return fail(GDN_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", fn,
                 workspace_bytes, need);
-  int *err = nullptr;
-  gdn_status st = device_err_ptr(&err);
-  if (st != GDN_OK) return st;
-
-  gdn::ChunkedArgs a{};
-  a.cu_seqlens = cu_seqlens;
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
-  a.state_in = state_in; a.slots = state_slots; a.out = out;
-  a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
-  a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
-  a.bf16 = s.in_dtype == GDN_BF16;
-  a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
-  a.kda = mode == GDN_MODE_KDA;
-  a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
+  if ((st = device_err_ptr(&a.err)) != GDN_OK) return st;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
   a.ckpt = ckpt; a.ckpt_every = ckpt_every; a.max_ckpts = max_ckpts;
-  a.err = err;
   return check_launch(gdn::launch_chunked(a, reinterpret_cast<cudaStream_t>(stream)),
                       fn);
 }
@@ -320,62 +332,18 @@ gdn_status gdn_forward_chunked_noalloc(const gdn_varlen_shape *shape,
                                        float *state_slots, float *out, int n_slots,
                                        gdn_mode mode, gdn_stream_t stream) {
   const char *fn = "gdn_forward_chunked_noalloc";
-  if (!shape) return fail(GDN_ERR_INVALID_ARG, "%s: shape is NULL", fn);
-  const gdn_varlen_shape &s = *shape;
-  if (s.n_seqs <= 0 || s.total_tokens < 0 || s.H <= 0)
-    return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs=%d total_tokens=%d H=%d", fn, s.n_seqs,
-                s.total_tokens, s.H);
-  if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
-    return fail(GDN_ERR_INVALID_ARG, "%s: mode %d", fn, (int)mode);
-  if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
-    return fail(GDN_ERR_INVALID_ARG, "%s: in_dtype %d", fn, (int)s.in_dtype);
-  if (n_slots < 1) return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d (need >= 1)", fn, n_slots);
-  if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
-    return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes D_k=%d D_v=%d (supported: 64, 128)", fn,
-                s.D_k, s.D_v);
-  if (!std::isfinite(s.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
-  int hq = 0;
-  if (qk_heads(fn, s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
-  if ((long long)s.total_tokens * s.H > (1LL << 31))
-    return fail(GDN_ERR_UNSUPPORTED, "%s: too many token-heads", fn);
-  const void *ptrs[] = {cu_seqlens, state_in, state_slots};
-  const char *names[] = {"cu_seqlens", "state_in", "state_slots"};
-  for (int i = 0; i < 3; ++i)
-    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
-  if (s.total_tokens > 0) {
-    const void *tp[] = {q, k, v, g, beta, out};
-    const char *tn[] = {"q", "k", "v", "g", "beta", "out"};
-    for (int i = 0; i < 6; ++i) {
-      if (!tp[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, tn[i]);
-      if (!aligned16(tp[i]))
-        return fail(GDN_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, tn[i]);
-    }
-  }
-  if (!aligned16(state_in) || !aligned16(state_slots) || !aligned16(cu_seqlens))
-    return fail(GDN_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", fn);
-  const size_t need = gdn::chunked_workspace_need(s.n_seqs, s.total_tokens, s.H, s.D_k,
-                                                  s.D_v, mode == GDN_MODE_KDA,
-                                                  s.in_dtype == GDN_BF16);
+  gdn::ChunkedArgs a;
+  gdn_status st = chunked_args(fn, shape, cu_seqlens, q, k, v, g, beta, state_in, state_slots,
+                               out, n_slots, mode, &a);
+  if (st != GDN_OK) return st;
+  const size_t need = gdn::chunked_workspace_need(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv,
+                                                  a.kda, a.bf16);
   if (need > gdn::static_scratch_bytes())
     return fail(GDN_ERR_UNSUPPORTED,
                 "%s: this shape needs %zu bytes of scratch; the built-in area holds %zu "
                 "(use gdn_forward_chunked with a workspace)",
                 fn, need, gdn::static_scratch_bytes());
-  int *err = nullptr;
-  gdn_status st = device_err_ptr(&err);
-  if (st != GDN_OK) return st;
-
-  gdn::ChunkedArgs a{};
-  a.cu_seqlens = cu_seqlens;
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
-  a.state_in = state_in; a.slots = state_slots; a.out = out;
-  a.n_seqs = s.n_seqs; a.total_tokens = s.total_tokens; a.H = s.H;
-  a.Hqk = hq; a.qk_grouped = s.qk_map == GDN_QK_GROUPED;
-  a.bf16 = s.in_dtype == GDN_BF16;
-  a.Dk = s.D_k; a.Dv = s.D_v; a.n_slots = n_slots;
-  a.kda = mode == GDN_MODE_KDA;
-  a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
-  a.err = err;
+  if ((st = device_err_ptr(&a.err)) != GDN_OK) return st;
   size_t need2 = 0;
   return check_launch(
       gdn::launch_chunked_static(a, reinterpret_cast<cudaStream_t>(stream), &need2), fn);
@@ -463,6 +431,53 @@ gdn_status gdn_slot_state_ptr(const float *state_slots, int seq, int slot,
   return GDN_OK;
 }
 
+static const char *wait_site_name(int site) {
+  switch (site) {
+    case gdn::kSiteRecTile: return "recurrent kernel, token tile copies";
+    case gdn::kSitePrepLoad: return "chunk prep, K/Q tile copies";
+    case gdn::kSitePrepG: return "chunk prep, G product";
+    case gdn::kSitePrepW: return "chunk prep, W product";
+    case gdn::kSiteScanX: return "chunk scan, X product";
+    case gdn::kSiteScanS: return "chunk scan, state-update product";
+    case gdn::kSiteScanO: return "chunk scan, output product";
+    case gdn::kSiteScanEmpty: return "chunk scan, stage release";
+    case gdn::kSiteScanPad: return "chunk scan, partial-chunk copies";
+    case gdn::kSiteScanStage: return "chunk scan, stage copies";
+    case gdn::kSiteScanS0: return "chunk scan, state operand";
+    case gdn::kSiteScanD: return "chunk scan, D tile";
+    default: return "unnamed wait";
+  }
+}
+
+gdn_status gdn_decode_device_error(int word) {
+  if (word == 0) return GDN_OK;
+  switch (word & 0xff) {
+    case gdn::kDevTimeout: {
+      const int site = (word >> 8) & 0xff;
+      return fail(GDN_ERR_TIMEOUT,
+                  "a device-side wait ran out (kernel abandoned its work; site %d: %s; "
+                  "chunk %d)",
+                  site, wait_site_name(site), (word >> 16) & 0x7fff);
+    }
+    case gdn::kDevBadSeqlens:
+      return fail(GDN_ERR_DEVICE_ARG, "cu_seqlens is not a valid offset table");
+    case gdn::kDevOverlap:
+      return fail(GDN_ERR_DEVICE_ARG, "a state_in pointer points into state_slots");
+    case gdn::kDevGateRange:
+      return fail(GDN_ERR_DEVICE_ARG,
+                  "a gate decays (or grows) by more than e^80 inside one 64-token chunk, or "
+                  "is NaN; the chunked path cannot represent that decay, run these "
+                  "sequences through gdn_forward");
+    default:
+      return fail(GDN_ERR_DEVICE_ARG, "device error word %d", word);
+  }
+}
+
+gdn_status gdn_device_error_word(int **word) {
+  if (!word) return fail(GDN_ERR_INVALID_ARG, "gdn_device_error_word: word is NULL");
+  return device_err_ptr(word);
+}
+
 gdn_status gdn_check_device_error(gdn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
@@ -479,23 +494,7 @@ gdn_status gdn_check_device_error(gdn_stream_t stream) {
   e = cudaMemcpyToSymbol(g_gdn_err_word, &zero, sizeof(int));
   if (e != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn_check_device_error: %s", cudaGetErrorString(e));
-  switch (word & 0xff) {
-    case gdn::kDevTimeout:
-      return fail(GDN_ERR_TIMEOUT,
-                  "a device-side wait ran out (kernel abandoned its work; site %d, chunk %d)",
-                  (word >> 8) & 0xff, (word >> 16) & 0x7fff);
-    case gdn::kDevBadSeqlens:
-      return fail(GDN_ERR_DEVICE_ARG, "cu_seqlens is not a valid offset table");
-    case gdn::kDevOverlap:
-      return fail(GDN_ERR_DEVICE_ARG, "a state_in pointer points into state_slots");
-    case gdn::kDevGateRange:
-      return fail(GDN_ERR_DEVICE_ARG,
-                  "a gate decays (or grows) by more than e^80 inside one 64-token chunk; the "
-                  "chunked path cannot represent that decay, run these sequences through "
-                  "gdn_forward");
-    default:
-      return fail(GDN_ERR_DEVICE_ARG, "device error word %d", word);
-  }
+  return gdn_decode_device_error(word);
 }
 
 }  // extern "C"

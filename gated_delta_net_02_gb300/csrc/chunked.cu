@@ -262,7 +262,8 @@ constexpr int PREP_GAM = PREP_KB + 64 * XS_LD * 4;  // [64] f32 gamma (GDA)
 constexpr int PREP_TF = PREP_GAM + 256;             // [64] f32 column factor of T'
 constexpr int PREP_BETA = PREP_TF + 256;            // [64] f32
 constexpr int PREP_HSUM = PREP_BETA + 256;          // [2][128] f32 KDA half-chunk gate sums
-constexpr int PREP_BAR = PREP_HSUM + 1024;          // 3 mbarriers
+constexpr int PREP_LAST = PREP_HSUM + 1024;         // [64] int GDA last reset row (-1: none)
+constexpr int PREP_BAR = PREP_LAST + 256;           // 3 mbarriers
 constexpr int PREP_TSLOT = PREP_BAR + 24;
 constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;    // + alignment slack
 constexpr uint32_t PCOL_G = 0, PCOL_W = 0;          // TMEM columns (128 allocated; W reuses G's)
@@ -300,6 +301,8 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   float *stf = reinterpret_cast<float *>(sm + PREP_TF);
   float *sbeta = reinterpret_cast<float *>(sm + PREP_BETA);
   float *hsum = reinterpret_cast<float *>(sm + PREP_HSUM);
+  int *slast = reinterpret_cast<int *>(sm + PREP_LAST);
+  float *smin = hsum;  // GDA: running minimum of the cumulative gate [64]
   uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
   uint64_t *bar_g = bar_tma + 1, *bar_w = bar_tma + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PREP_TSLOT);
@@ -338,21 +341,48 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     const long long row = (long long)(t0 + tid) * H + h;
     sbeta[tid] = tid < len ? beta[row] : 0.f;
     if constexpr (!KDA) {
-      // inclusive cumulative gate: shuffle scan in each warp, then warp 1
-      // adds warp 0's total
+      // A gate of -inf resets the state: every decay across that token is
+      // exactly zero. The cumulative gate sums the other (finite) gates, and
+      // slast[r] is the last reset row <= r (-1: none), so the decay from
+      // row j to row r >= j is zero when slast[r] > j and e^(sgam[r] -
+      // sgam[j]) otherwise, never inf - inf. Inclusive shuffle scans (sum
+      // and max) in each warp, then warp 1 adds warp 0's totals.
       float x = tid < len ? g[row] : 0.f;
+      int li = -1;
+      if (x == -INFINITY) {
+        x = 0.f;
+        li = tid;
+      }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
+        const int l = __shfl_up_sync(0xffffffffu, li, off);
+        if (lane >= off) {
+          x += y;
+          li = max(li, l);
+        }
+      }
+      // running minimum of the cumulative gate (warp 0 also counts the chunk
+      // start, 0), for the growth check below
+      float mn = tid < 32 ? fminf(x, 0.f) : x;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, mn, off);
+        if (lane >= off) mn = fminf(mn, y);
       }
       sgam[tid] = x;
+      slast[tid] = li;
+      smin[tid] = mn;
     }
   }
-  if (tid == 0 && !mbar_wait(bar_tma, 0, err, 1)) abort_flag = 1;
+  if (tid == 0 && !mbar_wait(bar_tma, 0, err, kSitePrepLoad)) abort_flag = 1;
   __syncthreads();
   if constexpr (!KDA) {
-    if (tid >= 32 && tid < CH) sgam[tid] += sgam[31];
+    if (tid >= 32 && tid < CH) {
+      smin[tid] = fminf(smin[31], smin[tid] + sgam[31]);
+      sgam[tid] += sgam[31];
+      slast[tid] = max(slast[tid], slast[31]);
+    }
   }
   if (abort_flag) return;
   if (len < CH) {  // padding rows of K and Q are zero
@@ -376,13 +406,14 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     __nv_bfloat16 *qh = w.Qh + tile * CH * DK + i;
     __nv_bfloat16 *kt = w.Kt + tile * CH * DK + i;
     float gam = half ? hsum[i] : 0.f;
-    float gabs = fabsf(gC);
+    // out of range (NaN included): |gamma| > 80 at the chunk end or any row
+    bool bad = !(fabsf(gC) <= kMaxChunkLogDecay);
     const float eC = __expf(gC);
 #pragma unroll
     for (int rr = 0; rr < HR; ++rr) {
       const int r = r0 + rr;
       gam += gcol[rr];
-      gabs = fmaxf(gabs, fabsf(gam));
+      bad |= !(fabsf(gam) <= kMaxChunkLogDecay);
       // |gamma| <= 80 inside a chunk (checked below), so e^gC e^-gamma does
       // not overflow and stands in for e^(gC - gamma)
       const float e1 = __expf(gam), e2 = __expf(-gam), e3 = eC * e2;
@@ -402,23 +433,27 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       w.gs[tile * 256 + 128 + i] = expf(gC);
       w.gs[tile * 256 + i] = 1.f;
     }
-    if (gabs > kMaxChunkLogDecay) set_error(err, kDevGateRange);
+    if (bad) set_error(err, kDevGateRange);
   } else {  // gate factors of the scan
     const float gCs = sgam[CH - 1];
+    const int lastC = slast[CH - 1];
     float *gs = w.gs + tile * 256;
     if (tid < CH) {
-      gs[tid] = expf(sgam[tid]);
-      gs[CH + tid] = expf(gCs - sgam[tid]);
-      // decays are exact pairwise differences; only growth can overflow
-      if (sgam[tid] > kMaxChunkLogDecay || gCs - sgam[tid] > kMaxChunkLogDecay)
-        set_error(err, kDevGateRange);
+      // decay from the chunk start to row tid, and from row tid to the end
+      gs[tid] = slast[tid] >= 0 ? 0.f : expf(sgam[tid]);
+      gs[CH + tid] = lastC > tid ? 0.f : expf(gCs - sgam[tid]);
+      // Decays are pairwise differences; only growth can overflow. The
+      // largest growth over rows (j, tid] is sgam[tid] minus smin[tid], the
+      // smallest cumulative gate up to it (0 at the chunk start); a NaN or
+      // +inf gate fails the test too.
+      if (!(sgam[tid] - smin[tid] <= kMaxChunkLogDecay)) set_error(err, kDevGateRange);
     } else if (tid < CH + 128) {
-      gs[128 + tid - CH] = expf(gCs);
+      gs[128 + tid - CH] = lastC >= 0 ? 0.f : expf(gCs);
     }
   }
   if (tid < CH) {  // column factor of T' = T diag(e^gamma) (GDA) or T (KDA)
     float f = sbeta[tid];
-    if constexpr (!KDA) f *= __expf(sgam[tid]);
+    if constexpr (!KDA) f = slast[tid] >= 0 ? 0.f : f * __expf(sgam[tid]);
     stf[tid] = f;
   }
   fence_proxy_async();
@@ -442,7 +477,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_G, sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u),
                 sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u), idesc, s > 0);
     umma_commit(bar_g);
-    if (!mbar_wait(bar_g, 0, err, 2)) abort_flag = 1;
+    if (!mbar_wait(bar_g, 0, err, kSitePrepG)) abort_flag = 1;
   }
   __syncthreads();
   tc_fence_after();
@@ -457,11 +492,12 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       const int r = row;
       const float br = sbeta[r];
       const float gr = KDA ? 0.f : sgam[r];
+      const int lr = KDA ? -1 : slast[r];  // decays across a reset row are zero
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int j = j0 + u;
         float a = 0.f;
-        if (j < r) {
+        if (j < r && j >= lr) {
           a = br * G[u];
           if constexpr (!KDA) a *= __expf(gr - sgam[j]);
         }
@@ -470,17 +506,18 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     } else {
       const int r = row - CH;
       const float gr = KDA ? 0.f : sgam[r];
+      const int lr = KDA ? -1 : slast[r];
       uint32_t packed[16];
 #pragma unroll
       for (int u = 0; u < 32; u += 2) {
         const int j = j0 + u;
         float p0 = 0.f, p1 = 0.f;
         if (r < len) {
-          if (j <= r) {
+          if (j <= r && j >= lr) {
             p0 = G[u];
             if constexpr (!KDA) p0 *= __expf(gr - sgam[j]);
           }
-          if (j + 1 <= r) {
+          if (j + 1 <= r && j + 1 >= lr) {
             p1 = G[u + 1];
             if constexpr (!KDA) p1 *= __expf(gr - sgam[j + 1]);
           }
@@ -591,7 +628,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_W, sdesc_kmajor(smem_u32(TZ) + s * 32),
                 sdesc_mnmajor(smem_u32(KQ) + s * 2048, 16384), idesc, s > 0);
     umma_commit(bar_w);
-    if (!mbar_wait(bar_w, 0, err, 3)) abort_flag = 1;
+    if (!mbar_wait(bar_w, 0, err, kSitePrepW)) abort_flag = 1;
   }
   __syncthreads();
   tc_fence_after();
@@ -810,7 +847,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       const int st = jc & 1;
       if (jc >= 2) {  // the products of chunk jc - 2 have released the stage
         int ok = 1;
-        if (lane == 0) ok = wait_ab(&empty[st], ((jc >> 1) - 1) & 1, abort_flag, err, 41, jc);
+        if (lane == 0) ok = wait_ab(&empty[st], ((jc >> 1) - 1) & 1, abort_flag, err, kSiteScanEmpty, jc);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
       unsigned char *base = sm + st * ST_BYTES;
@@ -865,7 +902,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         // (rows of K^T D~). Padding rows of Q only reach outputs that are
         // not stored; KDA's K~ and Q^ come from the workspace, already padded.
         int ok = 1;
-        if (lane == 0) ok = wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, 42, jc);
+        if (lane == 0) ok = wait_ab(&full[st], (jc >> 1) & 1, abort_flag, err, kSiteScanPad, jc);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         constexpr int per_row = KDA ? 8 : 24;  // 16-byte pieces per padding row
         for (int e = lane; e < (CH - len) * per_row; e += 32) {
@@ -925,7 +962,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       // X(j) += [-W; Q] S0, once S0 is in shared memory
       auto issue_x2 = [&](int j) -> bool {
         const uint32_t colx = COL_X0 + 64u * (uint32_t)(j % 3);
-        if (!wait_ab(bE4, j & 1, abort_flag, err, 53, j)) return false;
+        if (!wait_ab(bE4, j & 1, abort_flag, err, kSiteScanS0, j)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k8 = 0; k8 < 8; ++k8)
@@ -936,7 +973,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       };
       uint32_t par;
       uint64_t *sb = stage_bar(0, &par);
-      bool ok = wait_ab(sb, par, abort_flag, err, 52, 0);
+      bool ok = wait_ab(sb, par, abort_flag, err, kSiteScanStage, 0);
       if (ok) {
         issue_x1(0);
         ok = issue_x2(0);
@@ -961,7 +998,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         }
         if (!d_ready || *abort_flag) {
           if (!d_ready && !*abort_flag) {
-            set_error(err, kDevTimeout | (54 << 8) | ((jc & 0x7fff) << 16));
+            set_error(err, kDevTimeout | (kSiteScanD << 8) | ((jc & 0x7fff) << 16));
             *abort_flag = 1;
           }
           break;
@@ -982,7 +1019,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         umma_commit(&empty[st]);
         if (jc + 1 < nch) {
           if (!x1_done) {
-            if (!wait_ab(nb, par, abort_flag, err, 52, jc + 1)) break;
+            if (!wait_ab(nb, par, abort_flag, err, kSiteScanStage, jc + 1)) break;
             issue_x1(jc + 1);
           }
           if (!issue_x2(jc + 1)) break;
@@ -1065,7 +1102,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     for (int jc = 0; jc < nch; ++jc) {
       const int st = jc & 1;
       const uint32_t colx = COL_X0 + 64u * (uint32_t)(jc % 3);
-      if (!rs.wait(tid == 0, bE5, jc & 1, abort_flag, err, 31, jc)) break;
+      if (!rs.wait(tid == 0, bE5, jc & 1, abort_flag, err, kSiteScanX, jc)) break;
       tc_fence_after();
       // gate factors of this chunk: the stage landed before X could finish;
       // the wait gives each thread its own view of it (never blocks here)
@@ -1098,7 +1135,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       named_bar(1);
       if (tid == 0) mbar_arrive(bE6);
       // state update, handed to the next chunk
-      if (!rs.wait(tid == 0, bE7, jc & 1, abort_flag, err, 32, jc)) break;
+      if (!rs.wait(tid == 0, bE7, jc & 1, abort_flag, err, kSiteScanS, jc)) break;
       tc_fence_after();
       {
         float v[32];
@@ -1126,7 +1163,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       // this chunk's outputs, while the next chunk's X is computed (the
       // staging tile is free once thread 0's earlier stores have read it)
       if (tid == 0) bulk_wait_read();
-      if (!rs.wait(tid == 0, &bE8[jc & 1], (jc >> 1) & 1, abort_flag, err, 34, jc)) break;
+      if (!rs.wait(tid == 0, &bE8[jc & 1], (jc >> 1) & 1, abort_flag, err, kSiteScanO, jc)) break;
       tc_fence_after();
       store_out(jc, qf);
       tc_fence_before();

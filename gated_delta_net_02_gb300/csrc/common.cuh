@@ -18,6 +18,23 @@ enum DevErr : int {
   kDevGateRange = 4,   // a chunk's cumulative log-gate leaves [-80, 80] (chunked path)
 };
 
+// Where a bounded wait ran out: bits 8..15 of a timeout error word. The host
+// names each site in the message of gdn_check_device_error.
+enum WaitSite : int {
+  kSiteRecTile = 11,      // recurrent kernel: token tile copies
+  kSitePrepLoad = 21,     // chunk prep: K and Q tile copies
+  kSitePrepG = 22,        // chunk prep: G product
+  kSitePrepW = 23,        // chunk prep: W product
+  kSiteScanX = 31,        // chunk scan, state warps: X product
+  kSiteScanS = 32,        // chunk scan, state warps: state-update product
+  kSiteScanO = 34,        // chunk scan, state warps: output product
+  kSiteScanEmpty = 41,    // chunk scan, producer: a stage released by its products
+  kSiteScanPad = 42,      // chunk scan, producer: copies of a partial last chunk
+  kSiteScanStage = 52,    // chunk scan, MMA issuer: a stage's copies
+  kSiteScanS0 = 53,       // chunk scan, MMA issuer: the state operand
+  kSiteScanD = 54,        // chunk scan, MMA issuer: the D tile
+};
+
 // Largest |cumulative log-gate| inside one chunk that the chunked kernels
 // accept: their decay factors e^(+-gamma) are stored in bf16/fp32, whose
 // range ends near e^88.
@@ -89,15 +106,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, polling at most kMaxPolls
+// Waits for phase `parity` of `bar` to complete, polling at most max_polls
 // times. Returns false (and sets the error word, with `site` in bits 8..15)
 // if the wait ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          int *err, int site = 0) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
+__device__ __forceinline__ bool mbar_wait_n(uint64_t *bar, uint32_t parity, int *err,
+                                            int site, uint32_t max_polls) {
+  for (uint32_t i = 0; i < max_polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   set_error(err, kDevTimeout | (site << 8));
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          int *err, int site = 0) {
+  return mbar_wait_n(bar, parity, err, site, kMaxPolls);
 }
 
 // Orders this thread's generic-proxy shared-memory accesses before later

@@ -222,27 +222,9 @@ __global__ void __launch_bounds__(C::NT)
   // Launched programmatically (gdn_forward), this grid may have been scheduled
   // while the previous kernel of the stream runs: nothing in global memory
   // has been read or written up to here (T and the token offsets are launch
-  // parameters then), and nothing is before that kernel completes. Without
-  // a programmatic launch the wait returns at once.
-  if (p.pdl && p.T >= 2) {
-    // Multi-token calls (speculative verify), while the previous kernel
-    // finishes: L2 prefetches of this CTA's state rows (measured: verify
-    // 50.35 -> 49.45 us per call; single-token decode got slower, 23.35 ->
-    // 23.90 us, and does without). A prefetch changes no value and L2 is where global memory is
-    // coherent, so rows that kernel is still writing are read correctly by
-    // the loads after the wait. The pointer is read at L2 only (no L1 line
-    // that the read after the wait could hit).
-    const float *spec = reinterpret_cast<const float *>(
-        __ldcg(reinterpret_cast<const unsigned long long *>(p.state_in + s)));
-    if (spec) {
-      const char *base =
-          reinterpret_cast<const char *>(spec + (long long)h * DK * DV + col_base);
-      for (int r = tid; r < DK; r += C::NT)
-#pragma unroll
-        for (int b = 0; b < CCOLS * 4; b += 128)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (long long)r * DV * 4 + b));
-    }
-  }
+  // parameters then), and nothing is before that kernel completes, not even
+  // an address to prefetch from (that kernel may be writing the state_in
+  // pointer array). Without a programmatic launch the wait returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // token copies and gate scalars first, then the state pointer
   if (warp == 0) issue(0, 0);
@@ -287,7 +269,7 @@ __global__ void __launch_bounds__(C::NT)
     if (warp == 0 && tile + 1 < ntiles) issue(tile + 1, b ^ 1);
     float g_nxt = 0.f, b_nxt = 0.f;
     if (tile + 1 < ntiles) gate_scalars(tile + 1, g_nxt, b_nxt);
-    if (tid == 0 && !mbar_wait(&bar[b], parity, p.err, 3)) abort_flag = 1;
+    if (tid == 0 && !mbar_wait(&bar[b], parity, p.err, kSiteRecTile)) abort_flag = 1;
     if (tid < n) {
       if constexpr (!C::KDA) fa[tid] = expf(g_cur);
       fb[tid] = b_cur;

@@ -100,6 +100,10 @@ lib.gdn_slot_state_ptr.restype = _st
 lib.gdn_slot_state_ptr.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_vp)]
 lib.gdn_check_device_error.restype = _st
 lib.gdn_check_device_error.argtypes = [_vp]
+lib.gdn_decode_device_error.restype = _st
+lib.gdn_decode_device_error.argtypes = [_i]
+lib.gdn_device_error_word.restype = _st
+lib.gdn_device_error_word.argtypes = [ctypes.POINTER(_vp)]
 
 
 def _addr(x):
@@ -203,6 +207,19 @@ def gdn_noalloc_scratch_bytes() -> int:
 
 def gdn_check_device_error(stream=None) -> None:
     _check(lib.gdn_check_device_error(_stream(stream)))
+
+
+def gdn_decode_device_error(word: int):
+    """(status, message) the library gives for a device error-word value."""
+    st = int(lib.gdn_decode_device_error(int(word)))
+    return st, (lib.gdn_last_error().decode(errors="replace") if st != GDN_OK else "")
+
+
+def gdn_device_error_word() -> int:
+    """Device address of the current device's error word."""
+    out = _vp()
+    _check(lib.gdn_device_error_word(ctypes.byref(out)))
+    return out.value or 0
 
 
 class SeqTable:

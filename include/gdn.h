@@ -300,6 +300,25 @@ gdn_status gdn_slot_state_ptr(const float *state_slots, int seq, int slot,
  * ---------------------------------------------------------------------- */
 gdn_status gdn_check_device_error(gdn_stream_t stream);
 
+/*
+ * Maps a value of the device error word to the status gdn_check_device_error
+ * returns for it, and sets the calling thread's gdn_last_error message to the
+ * text it would give: GDN_OK for 0; GDN_ERR_TIMEOUT for a bounded wait that
+ * ran out (the message names the wait site, bits 8..15, and the chunk, bits
+ * 16..30); GDN_ERR_DEVICE_ARG for the argument conditions above. Host only,
+ * no device access.
+ */
+gdn_status gdn_decode_device_error(int word);
+
+/*
+ * Device address of the current device's error word (one int), for a
+ * caller's own kernels that want to report through gdn_check_device_error:
+ * they set it with atomicCAS(word, 0, value) so that the first condition
+ * wins, as the library's kernels do. The address is looked up once per
+ * device and is not valid after cudaDeviceReset.
+ */
+gdn_status gdn_device_error_word(int **word);
+
 #ifdef __cplusplus
 }
 #endif

@@ -196,3 +196,34 @@ def test_binding_refuses_strided_views(gdn):
         gdn._addr(x.t())
     assert gdn._addr(x) == x.data_ptr()
     assert gdn._addr(None) is None and gdn._addr(1 << 20) == 1 << 20
+
+
+def wait_sites():
+    src = open(os.path.join(ROOT, "gated_delta_net_02_gb300", "csrc", "common.cuh")).read()
+    return {name: int(v) for name, v in re.findall(r"(kSite\w+) = (\d+)", src)}
+
+
+def test_device_error_word_decoding(gdn):
+    """Every value the kernels can put in the error word maps to its status
+    and message, with no device access: timeouts name their wait site
+    (bits 8..15) and chunk (bits 16..30); each named site has its own name."""
+    assert gdn.gdn_decode_device_error(0) == (gdn.GDN_OK, "")
+    sites = wait_sites()
+    assert len(sites) >= 10 and len(set(sites.values())) == len(sites)
+    names = set()
+    for site in sites.values():
+        st, msg = gdn.gdn_decode_device_error(1 | (site << 8) | (37 << 16))
+        assert st == gdn.GDN_ERR_TIMEOUT
+        assert f"site {site}: " in msg and "chunk 37" in msg and "unnamed" not in msg
+        names.add(msg.split(f"site {site}: ")[1].split(";")[0])
+    assert len(names) == len(sites)
+    st, msg = gdn.gdn_decode_device_error(1 | (250 << 8))
+    assert st == gdn.GDN_ERR_TIMEOUT and "site 250: unnamed wait" in msg
+    assert gdn.gdn_decode_device_error(2) == (gdn.GDN_ERR_DEVICE_ARG,
+                                              "cu_seqlens is not a valid offset table")
+    st, msg = gdn.gdn_decode_device_error(3)
+    assert st == gdn.GDN_ERR_DEVICE_ARG and "state_slots" in msg
+    st, msg = gdn.gdn_decode_device_error(4)
+    assert st == gdn.GDN_ERR_DEVICE_ARG and "e^80" in msg and "gdn_forward" in msg
+    st, msg = gdn.gdn_decode_device_error(9)
+    assert st == gdn.GDN_ERR_DEVICE_ARG and "device error word 9" in msg

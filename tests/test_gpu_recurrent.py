@@ -89,6 +89,49 @@ def test_decode_full_size_chained_steps(gdn):
     assert rel_l2(dst.double().cpu().numpy(), S_ref) < 1e-5
 
 
+def test_decode_1000_step_chain_against_oracle(gdn):
+    """The batched decode workload in full: 64 sequences x 1 token, H=16,
+    D=128, bf16 q/k/v, GDA, state ~N(0, 0.05), 1000 consecutive steps with
+    fresh tokens, each step reading the state the previous step wrote. The
+    oracle runs the same chain (the 1000 steps of a sequence are its tokens),
+    100 steps per call; every step's output and the state after every 100th
+    step are compared."""
+    import oracle
+    N, H, D, STEPS, BLOCK = 64, 16, 128, 1000, 100
+    state0 = inputs.decode_state(1, N, H, D)
+    bank = [state0.cuda(), torch.empty(N, H, D, D, device="cuda")]
+    ptrs = [gdn.state_ptr_array(gdn.per_seq_state_ptrs(b_, N), "cuda") for b_ in bank]
+    shape = gdn.gdn_shape(N, 1, H, D, D, gdn.GDN_BF16, D ** -0.5)
+    S_ref = inputs.to_f64(state0)
+    worst_out = worst_state = 0.0
+    for blk in range(STEPS // BLOCK):
+        toks = [inputs.decode_tokens(1, blk * BLOCK + t, N, H, D) for t in range(BLOCK)]
+        dev = [[x.cuda() for x in tk] for tk in toks]
+        outs = torch.empty(BLOCK, N, H, D, device="cuda")
+        for t in range(BLOCK):
+            i = blk * BLOCK + t
+            q, k, v, g, beta = dev[t]
+            gdn.gdn_forward(shape, q, k, v, g, beta, ptrs[i % 2], bank[(i + 1) % 2], outs[t],
+                            1, "gda")
+        gdn.gdn_check_device_error()
+        # the oracle: sequence s's tokens are steps t of this block, packed
+        # sequence by sequence
+        seq = [torch.stack([tk[j] for tk in toks], dim=1) for j in range(5)]   # [N, T, ...]
+        q, k, v, g, beta = (inputs.to_f64(x.reshape(N * BLOCK, *x.shape[2:])) for x in seq)
+        o_ref, S_ref, _ = oracle.forward(q, k, v, g, beta, S_ref, scale=D ** -0.5,
+                                         seq_start=np.arange(N) * BLOCK,
+                                         seq_len=np.full(N, BLOCK))
+        got = outs.permute(1, 0, 2, 3).reshape(N * BLOCK, H, D).double().cpu().numpy()
+        e_out = rel_l2(got, o_ref)
+        e_st = rel_l2(bank[((blk + 1) * BLOCK) % 2].double().cpu().numpy(), S_ref)
+        worst_out, worst_state = max(worst_out, e_out), max(worst_state, e_st)
+        assert e_out <= 5e-3 and e_st <= 5e-3, (blk, e_out, e_st)
+    print(f"decode 1000-step chain: worst out rel-L2 {worst_out:.2e}, "
+          f"worst state rel-L2 {worst_state:.2e}")
+    # fp32 arithmetic on exact bf16 inputs: far inside the bf16 budget
+    assert worst_state < 1e-5
+
+
 def test_verify_full_size_and_rollback_bit_exact(gdn):
     """32 sequences x T=8, K=8, H=16, D=128, bf16: parity, then rollback to
     n_accepted ~ U{0..8} and a re-run of only the accepted prefix from the
@@ -206,9 +249,9 @@ def test_runs_on_a_side_stream(gdn):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("n_slots", [1, 3])
 def test_decode_step_bitwise_equals_first_token_of_longer_run(gdn, mode, dtype, n_slots):
-    """A decode step (T = 1, the persistent decode kernel for 128 x 128 heads)
-    must reproduce, bit for bit, token 0 of a T = 2 run from the same state
-    (the tile kernel): the per-token arithmetic is shared."""
+    """A decode step (T = 1) must reproduce, bit for bit, token 0 of a T = 2
+    run from the same state: the recurrent kernel's per-token arithmetic and
+    its reduction order do not depend on T or on the number of slots."""
     b2 = inputs.make_batch(200 + n_slots, [2] * 5, 3, 128, 128, dtype=dtype, mode=mode,
                            n_slots=2)
     d2 = to_dev(b2)
@@ -225,7 +268,7 @@ def test_decode_step_bitwise_equals_first_token_of_longer_run(gdn, mode, dtype, 
 
 
 def test_decode_step_null_state_and_few_items(gdn):
-    # 1 sequence x 1 head: fewer work items than persistent CTAs; NULL state
+    # 1 sequence x 1 head (a grid of two CTAs); NULL state pointer
     b = inputs.make_batch(210, [1], 1, 128, 128, state_std=0.0, n_slots=1)
     out_a, sl_a = gpu_forward(b)
     out_b, sl_b = gpu_forward(b, state_ptrs=gdn.state_ptr_array([0], "cuda"))
