@@ -153,6 +153,26 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
   return u;
 }
 
+// tf32 high part of x (round to nearest) and the tf32 rounding of the rest:
+// x = hi + lo up to the last bits of lo.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
+}
+
+// Warp-level D (16 x 8, fp32) += A (16 x 8, tf32, row-major) * B (8 x 8, tf32),
+// fragments as the PTX ISA lays out mma.m16n8k8 (g = lane / 4, t = lane % 4):
+// a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
+// d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // ---- 1. work list ---------------------------------------------------------------
 
 constexpr int WL_THREADS = 1024;
@@ -261,9 +281,11 @@ constexpr int PREP_KQ = 0, PREP_TZ = 8192, PREP_KB = 32768;
 constexpr int PREP_GAM = PREP_KB + 64 * XS_LD * 4;  // [64] f32 gamma (GDA)
 constexpr int PREP_TF = PREP_GAM + 256;             // [64] f32 column factor of T'
 constexpr int PREP_BETA = PREP_TF + 256;            // [64] f32
-constexpr int PREP_HSUM = PREP_BETA + 256;          // [2][128] f32 KDA half-chunk gate sums
+constexpr int PREP_HSUM = PREP_BETA + 256;          // [64] f32 GDA running gate minimum (1 KB)
 constexpr int PREP_LAST = PREP_HSUM + 1024;         // [64] int GDA last reset row (-1: none)
-constexpr int PREP_BAR = PREP_LAST + 256;           // 3 mbarriers
+constexpr int PREP_FAC = PREP_LAST + 256;           // GDA [64] row, [64] column decay factors,
+                                                    // [4] gate range, [1] factored flag
+constexpr int PREP_BAR = PREP_FAC + 512 + 32;       // 3 mbarriers
 constexpr int PREP_TSLOT = PREP_BAR + 24;
 constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;    // + alignment slack
 constexpr uint32_t PCOL_G = 0, PCOL_W = 0;          // TMEM columns (128 allocated; W reuses G's)
@@ -303,6 +325,9 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   float *hsum = reinterpret_cast<float *>(sm + PREP_HSUM);
   int *slast = reinterpret_cast<int *>(sm + PREP_LAST);
   float *smin = hsum;  // GDA: running minimum of the cumulative gate [64]
+  float *srowf = reinterpret_cast<float *>(sm + PREP_FAC), *scolf = srowf + 64;
+  float *srange = scolf + 64;
+  int *sfact = reinterpret_cast<int *>(srange + 4);
   uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
   uint64_t *bar_g = bar_tma + 1, *bar_w = bar_tma + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PREP_TSLOT);
@@ -325,17 +350,25 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     tma_load_3d(KQ + 16384 + 8192, &map_q, 64, hq, t0, bar_tma);
   }
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
-  constexpr int HR = CH / 2;  // KDA: thread (i, half) owns channel i, rows HR*half..
-  float gcol[KDA ? HR : 1];
+  // KDA gates, loaded while the tiles are in flight: thread = 8 channels
+  // (column chunk kc) x 4 consecutive rows (row group krg); the 16 row groups
+  // of a chunk are the 16 lanes of a half warp
+  const int kc = 2 * warp + (lane >> 4), krg = lane & 15;
+  float gk[KDA ? 4 : 1][8];
   if constexpr (KDA) {
-    const int i = tid & 127, r0 = HR * (tid >> 7);
-    float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < HR; ++r) {
-      gcol[r] = r0 + r < len ? g[((long long)(t0 + r0 + r) * H + h) * DK + i] : 0.f;
-      s += gcol[r];
+    for (int k = 0; k < 4; ++k) {
+      const int r = 4 * krg + k;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (r < len) {
+        const float4 *src =
+            reinterpret_cast<const float4 *>(g + ((long long)(t0 + r) * H + h) * DK + 8 * kc);
+        a = src[0];
+        b = src[1];
+      }
+      gk[k][0] = a.x; gk[k][1] = a.y; gk[k][2] = a.z; gk[k][3] = a.w;
+      gk[k][4] = b.x; gk[k][5] = b.y; gk[k][6] = b.z; gk[k][7] = b.w;
     }
-    hsum[(tid >> 7) * 128 + i] = s;
   }
   if (tid < CH) {
     const long long row = (long long)(t0 + tid) * H + h;
@@ -399,39 +432,75 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   if constexpr (KDA) {
     // Per-row decays inside the operands, relative to the chunk start:
     // K^ = e^g K and Q^ = e^g Q (A of G; K^ is also B of W), e^-g K (B of G),
-    // and for the scan Q^, K~ = e^(gC - g) K and e^gC.
-    const int i = tid & 127, half = tid >> 7, r0 = HR * half;
-    const float gC = hsum[i] + hsum[128 + i];
-    const uint32_t aoff = (uint32_t)(i >> 6) * 16384u, boff = (uint32_t)(i >> 6) * 8192u;
-    __nv_bfloat16 *qh = w.Qh + tile * CH * DK + i;
-    __nv_bfloat16 *kt = w.Kt + tile * CH * DK + i;
-    float gam = half ? hsum[i] : 0.f;
-    // out of range (NaN included): |gamma| > 80 at the chunk end or any row
-    bool bad = !(fabsf(gC) <= kMaxChunkLogDecay);
-    const float eC = __expf(gC);
+    // and for the scan Q^, K~ = e^(gC - g) K and e^gC. Cumulative gates:
+    // prefix over the thread's 4 rows, then over the 16 row groups of the
+    // chunk by shuffles within the half warp.
 #pragma unroll
-    for (int rr = 0; rr < HR; ++rr) {
-      const int r = r0 + rr;
-      gam += gcol[rr];
-      bad |= !(fabsf(gam) <= kMaxChunkLogDecay);
-      // |gamma| <= 80 inside a chunk (checked below), so e^gC e^-gamma does
-      // not overflow and stands in for e^(gC - gamma)
-      const float e1 = __expf(gam), e2 = __expf(-gam), e3 = eC * e2;
-      __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(r, i & 63));
-      __nv_bfloat16 *pq =
-          reinterpret_cast<__nv_bfloat16 *>(KQ + aoff + sw128_offset(CH + r, i & 63));
-      const float kv = __bfloat162float(*pk), qv = __bfloat162float(*pq);
-      const __nv_bfloat16 qhv = __float2bfloat16(qv * e1);
-      *pk = __float2bfloat16(kv * e1);
-      *pq = qhv;
-      *reinterpret_cast<__nv_bfloat16 *>(KB + boff + sw128_offset(r, i & 63)) =
-          __float2bfloat16(kv * e2);
-      qh[r * DK] = qhv;
-      kt[r * DK] = __float2bfloat16(kv * e3);
+    for (int k = 1; k < 4; ++k)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) gk[k][c] += gk[k - 1][c];
+    float gC[8], ex[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float x = gk[3][c];
+#pragma unroll
+      for (int d = 1; d < 16; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d, 16);
+        if (krg >= d) x += y;
+      }
+      ex[c] = x - gk[3][c];                               // rows before this group
+      gC[c] = __shfl_sync(0xffffffffu, x, 15, 16);        // whole chunk
     }
-    if (half == 0) {
-      w.gs[tile * 256 + 128 + i] = expf(gC);
-      w.gs[tile * 256 + i] = 1.f;
+    // out of range (NaN included): |gamma| > 80 at the chunk end or any row
+    bool bad = false;
+    float eC[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      bad |= !(fabsf(gC[c]) <= kMaxChunkLogDecay);
+      eC[c] = __expf(gC[c]);
+    }
+    const uint32_t half_off = (uint32_t)(kc >> 3) * 16384u, kb_off = (uint32_t)(kc >> 3) * 8192u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = 4 * krg + k;
+      const uint32_t sw = (uint32_t)((((kc & 7) ^ (r & 7)) << 4) + r * 128);
+      uint4 *pk = reinterpret_cast<uint4 *>(KQ + half_off + sw);
+      uint4 *pq = reinterpret_cast<uint4 *>(KQ + half_off + 8192 + sw);
+      const uint4 ku = *pk, qu = *pq;
+      const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ku);
+      const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qu);
+      float kh[8], qh[8], kb[8], kt[8];
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2) {
+        const float2 kf = __bfloat1622float2(k2[c2]), qf = __bfloat1622float2(q2[c2]);
+        const float kv[2] = {kf.x, kf.y}, qv[2] = {qf.x, qf.y};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * c2 + e;
+          const float gam = gk[k][c] + ex[c];
+          bad |= !(fabsf(gam) <= kMaxChunkLogDecay);
+          // |gamma| <= 80 inside a chunk (checked), so e^gC e^-gamma does not
+          // overflow and stands in for e^(gC - gamma)
+          const float e1 = __expf(gam), e2 = __expf(-gam);
+          kh[c] = kv[e] * e1;
+          qh[c] = qv[e] * e1;
+          kb[c] = kv[e] * e2;
+          kt[c] = kv[e] * (eC[c] * e2);
+        }
+      }
+      const uint4 qhu = pack8(qh);
+      *pk = pack8(kh);
+      *pq = qhu;
+      *reinterpret_cast<uint4 *>(KB + kb_off + sw) = pack8(kb);
+      *reinterpret_cast<uint4 *>(w.Qh + (tile * CH + r) * DK + 8 * kc) = qhu;
+      *reinterpret_cast<uint4 *>(w.Kt + (tile * CH + r) * DK + 8 * kc) = pack8(kt);
+    }
+    if (krg == 0) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        w.gs[tile * 256 + 128 + 8 * kc + c] = expf(gC[c]);
+        w.gs[tile * 256 + 8 * kc + c] = 1.f;
+      }
     }
     if (bad) set_error(err, kDevGateRange);
   } else {  // gate factors of the scan
@@ -447,6 +516,17 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       // smallest cumulative gate up to it (0 at the chunk start); a NaN or
       // +inf gate fails the test too.
       if (!(sgam[tid] - smin[tid] <= kMaxChunkLogDecay)) set_error(err, kDevGateRange);
+      // range of the cumulative gate over the chunk, for the factored decays
+      float hi = sgam[tid], lo = hi;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      }
+      if (lane == 0) {
+        srange[2 * warp] = hi;
+        srange[2 * warp + 1] = lo;
+      }
     } else if (tid < CH + 128) {
       gs[128 + tid - CH] = lastC >= 0 ? 0.f : expf(gCs);
     }
@@ -465,6 +545,20 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  if constexpr (!KDA) {
+    // Decay from row j to row r: e^(gamma_r - gamma_j) = e^(gamma_r - m) e^(m - gamma_j)
+    // with m the middle of the chunk's gate range. When that range is at most
+    // 160 both factors stay within e^(+-80) (no overflow, no flush to zero of a
+    // factor whose partner is large), and A and P take two multiplies per
+    // element instead of an exponential; wider ranges keep the pairwise form.
+    if (tid < CH) {
+      const float hi = fmaxf(srange[0], srange[2]), lo = fminf(srange[1], srange[3]);
+      const float m = 0.5f * (hi + lo);
+      srowf[tid] = __expf(sgam[tid] - m);
+      scolf[tid] = __expf(m - sgam[tid]);
+      if (tid == 0) *sfact = hi - lo <= 2.f * kMaxChunkLogDecay ? 1 : 0;
+    }
+  }
 
   // G = [K'; Q'] K''^T : M = 128, N = 64, K = 128 (8 steps of 16)
   if (tid == 0) {
@@ -493,36 +587,57 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       const float br = sbeta[r];
       const float gr = KDA ? 0.f : sgam[r];
       const int lr = KDA ? -1 : slast[r];  // decays across a reset row are zero
+      if (KDA || !*sfact) {
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const int j = j0 + u;
-        float a = 0.f;
-        if (j < r && j >= lr) {
-          a = br * G[u];
-          if constexpr (!KDA) a *= __expf(gr - sgam[j]);
+        for (int u = 0; u < 32; ++u) {
+          const int j = j0 + u;
+          float a = 0.f;
+          if (j < r && j >= lr) {
+            a = br * G[u];
+            if constexpr (!KDA) a *= __expf(gr - sgam[j]);
+          }
+          *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
         }
-        *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
+      } else {
+        const float brf = br * srowf[r];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int j = j0 + u;
+          const float a = j < r && j >= lr ? brf * G[u] * scolf[j] : 0.f;
+          *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
+        }
       }
     } else {
       const int r = row - CH;
       const float gr = KDA ? 0.f : sgam[r];
       const int lr = KDA ? -1 : slast[r];
       uint32_t packed[16];
+      if (KDA || !*sfact) {
 #pragma unroll
-      for (int u = 0; u < 32; u += 2) {
-        const int j = j0 + u;
-        float p0 = 0.f, p1 = 0.f;
-        if (r < len) {
-          if (j <= r && j >= lr) {
-            p0 = G[u];
-            if constexpr (!KDA) p0 *= __expf(gr - sgam[j]);
+        for (int u = 0; u < 32; u += 2) {
+          const int j = j0 + u;
+          float p0 = 0.f, p1 = 0.f;
+          if (r < len) {
+            if (j <= r && j >= lr) {
+              p0 = G[u];
+              if constexpr (!KDA) p0 *= __expf(gr - sgam[j]);
+            }
+            if (j + 1 <= r && j + 1 >= lr) {
+              p1 = G[u + 1];
+              if constexpr (!KDA) p1 *= __expf(gr - sgam[j + 1]);
+            }
           }
-          if (j + 1 <= r && j + 1 >= lr) {
-            p1 = G[u + 1];
-            if constexpr (!KDA) p1 *= __expf(gr - sgam[j + 1]);
-          }
+          packed[u / 2] = pack_bf16(p0, p1);
         }
-        packed[u / 2] = pack_bf16(p0, p1);
+      } else {
+        const float rf = r < len ? srowf[r] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const int j = j0 + u;
+          const float p0 = j <= r && j >= lr ? rf * G[u] * scolf[j] : 0.f;
+          const float p1 = j + 1 <= r && j + 1 >= lr ? rf * G[u + 1] * scolf[j + 1] : 0.f;
+          packed[u / 2] = pack_bf16(p0, p1);
+        }
       }
       uint4 *dst = reinterpret_cast<uint4 *>(w.P + (tile * CH + r) * CH + j0);
 #pragma unroll
@@ -538,60 +653,92 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     return;
   }
 
-  // X = (I + A)^-1 in fp32, X[r][c] = delta_rc - sum_{k<r} A[r][k] X[k][c],
-  // as a wavefront over 16-row blocks: thread (c, R) owns rows 16R..16R+15
-  // of column c. At step kb the owner of block kb finishes it by forward
-  // substitution; then every later block adds A(R, kb) X(kb, c). A rows are
-  // broadcast loads (all threads of a warp share R), X(kb, c) comes from
-  // shared memory.
+  // X = (I + A)^-1 by 16 x 16 blocks (A strictly lower triangular):
+  //   X[R][R] = (I + A[R][R])^-1,
+  //   X[R][K] = -X[R][R] sum_{M=K..R-1} A[R][M] X[M][K]      (K < R),
+  // one block row after another. The four diagonal inverses are forward
+  // substitutions on the CUDA cores (thread = block and column); the block
+  // products run on the tensor cores as warp-level tf32 MMAs with every
+  // operand split into a tf32 high and low part (hi*hi + hi*lo + lo*hi), which
+  // keeps them at fp32 accuracy. X goes to Xs (fp32, row stride XS_LD).
   {
-    const int cc = tid & 63, R = tid >> 6;
-    const uint32_t rowbase = (uint32_t)((R >> 1) * 16384 + 8192 + (R & 1) * 4096);
-    float acc[16];
+    if (tid < CH) {  // diagonal block R, column c: right-looking substitution
+      const int R = tid >> 4, c = tid & 15, r0 = 16 * R;
+      float acc[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) acc[u] = 0.f;
-    // X is lower triangular: for columns 32..63 (warps with cc >= 32) the
-    // blocks R = 0, 1 are zero and contribute nothing to later blocks
-    const int kb_lo = cc >= 32 ? 2 : 0;
-    for (int kb = 0; kb < 4; ++kb) {
-      if (R == kb && R < kb_lo) {  // an all-zero block of this column
+      for (int u = 0; u < 16; ++u) acc[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) Xs[(16 * R + u) * XS_LD + cc] = 0.f;
-      } else if (R == kb) {  // finish block R, right-looking
+      for (int u = 0; u < 16; ++u) {
+        const float xu = (u == c ? 1.f : 0.f) - acc[u];
+        Xs[(r0 + u) * XS_LD + r0 + c] = xu;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float xu = (16 * R + u == cc ? 1.f : 0.f) - acc[u];
-          Xs[(16 * R + u) * XS_LD + cc] = xu;
-#pragma unroll
-          for (int u2 = u + 1; u2 < 16; ++u2)
-            acc[u2] = fmaf(*reinterpret_cast<const float *>(KQ + rowbase + u2 * 256 + 64 * R +
-                                                            4 * (u ^ u2)),
-                           xu, acc[u2]);
-        }
+        for (int u2 = u + 1; u2 < 16; ++u2)
+          acc[u2] = fmaf(*reinterpret_cast<const float *>(KQ + af_off(r0 + u2, r0 + u)), xu,
+                         acc[u2]);
       }
-      __syncthreads();
-      if (R > kb && kb >= kb_lo) {  // contribution of the finished block kb
-#pragma unroll 1
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int k0 = 16 * kb + 4 * k4;
-          float x[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) x[b] = Xs[(k0 + b) * XS_LD + cc];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            // row r = 16R+u keeps A(r, k0 + b) at column 16kb + ((4k4 + b) ^ u):
-            // one float4 at 16kb + (4k4 ^ (u & 12)), element b in lane b ^ (u & 3)
-            const float4 a4 = *reinterpret_cast<const float4 *>(
-                KQ + rowbase + u * 256 + 64 * kb + 4 * ((4 * k4) ^ (u & 12)));
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[u] = fmaf(av[b ^ (u & 3)], x[b], acc[u]);
-          }
-        }
+    } else {  // zero blocks above the diagonal
+      for (int e = tid - CH; e < 6 * 256; e += PREP_THREADS - CH) {
+        const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+        // upper blocks (R, K), K > R: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int R = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int K = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Xs[(16 * R + rr) * XS_LD + 16 * K + cc] = 0.f;
       }
     }
+    __syncthreads();
+    const int g = lane >> 2, t = lane & 3;
+    for (int R = 1; R < 4; ++R) {
+      if (warp < 2 * R) {  // output X[R][K], columns 8 nh .. 8 nh + 7 of block K
+        const int K = warp >> 1, c0 = 16 * K + 8 * (warp & 1), r0 = 16 * R;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int M = K; M < R; ++M) {
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const int ka = 16 * M + 8 * ks;
+            uint32_t ah[4], al[4], bh[2], bl[2];
+            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g, ka + t)), ah[0], al[0]);
+            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g + 8, ka + t)), ah[1], al[1]);
+            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g, ka + t + 4)), ah[2], al[2]);
+            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g + 8, ka + t + 4)), ah[3],
+                       al[3]);
+            split_tf32(Xs[(ka + t) * XS_LD + c0 + g], bh[0], bl[0]);
+            split_tf32(Xs[(ka + t + 4) * XS_LD + c0 + g], bh[1], bl[1]);
+            mma_tf32(acc, al, bh);
+            mma_tf32(acc, ah, bl);
+            mma_tf32(acc, ah, bh);
+          }
+        }
+        // the sum over M goes where X[R][K] will be (this warp alone reads
+        // and writes these 16 x 8 values), then X[R][K] = -X[R][R] (sum)
+        Xs[(r0 + g) * XS_LD + c0 + 2 * t] = acc[0];
+        Xs[(r0 + g) * XS_LD + c0 + 2 * t + 1] = acc[1];
+        Xs[(r0 + g + 8) * XS_LD + c0 + 2 * t] = acc[2];
+        Xs[(r0 + g + 8) * XS_LD + c0 + 2 * t + 1] = acc[3];
+        __syncwarp();
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const int ka = r0 + 8 * ks;
+          uint32_t ah[4], al[4], bh[2], bl[2];
+          split_tf32(Xs[(r0 + g) * XS_LD + ka + t], ah[0], al[0]);
+          split_tf32(Xs[(r0 + g + 8) * XS_LD + ka + t], ah[1], al[1]);
+          split_tf32(Xs[(r0 + g) * XS_LD + ka + t + 4], ah[2], al[2]);
+          split_tf32(Xs[(r0 + g + 8) * XS_LD + ka + t + 4], ah[3], al[3]);
+          split_tf32(Xs[(ka + t) * XS_LD + c0 + g], bh[0], bl[0]);
+          split_tf32(Xs[(ka + t + 4) * XS_LD + c0 + g], bh[1], bl[1]);
+          mma_tf32(o, al, bh);
+          mma_tf32(o, ah, bl);
+          mma_tf32(o, ah, bh);
+        }
+        __syncwarp();  // every lane has read the sum before it is overwritten
+        Xs[(r0 + g) * XS_LD + c0 + 2 * t] = -o[0];
+        Xs[(r0 + g) * XS_LD + c0 + 2 * t + 1] = -o[1];
+        Xs[(r0 + g + 8) * XS_LD + c0 + 2 * t] = -o[2];
+        Xs[(r0 + g + 8) * XS_LD + c0 + 2 * t + 1] = -o[3];
+      }
+      __syncthreads();
+    }
   }
-  __syncthreads();
   // T[r][j] = X[r][j] beta_j (to the workspace) and T'[r][j] = X[r][j] f_j
   // into TZ; thread = (row r, 16 columns)
   {
