@@ -442,6 +442,7 @@ static const char *wait_site_name(int site) {
     case gdn::kSiteScanO: return "chunk scan, output product";
     case gdn::kSiteScanEmpty: return "chunk scan, stage release";
     case gdn::kSiteScanPad: return "chunk scan, partial-chunk copies";
+    case gdn::kSiteScanReady: return "chunk scan, ready flag of a prepared tile";
     case gdn::kSiteScanStage: return "chunk scan, stage copies";
     case gdn::kSiteScanS0: return "chunk scan, state operand";
     case gdn::kSiteScanD: return "chunk scan, D tile";

@@ -39,6 +39,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -59,7 +60,7 @@ constexpr int CH = 64;  // chunk length
 
 struct WsLayout {
   size_t hdr, chunk_seq, chunk_tok, chunk_len, seq_chunk0, seq_nch, tail_start,
-      tail_len, tail_pos, order, state_ptrs, states, T, P, W, Qh, Kt, gs, total;
+      tail_len, tail_pos, order, state_ptrs, states, ready, T, P, W, Qh, Kt, gs, total;
   long long max_chunks;
 };
 
@@ -90,6 +91,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
   w.order = take(sizeof(int) * (size_t)n_seqs);
   w.state_ptrs = take(sizeof(float *) * (size_t)n_seqs);
   w.states = take(with_tiles ? sizeof(float) * (size_t)n_seqs * H * Dk * Dv : 0);
+  w.ready = take(sizeof(int) * tiles);
   w.T = take(2 * tiles * CH * CH);
   w.P = take(2 * tiles * CH * CH);
   w.W = take(2 * tiles * CH * Dk);
@@ -103,6 +105,7 @@ WsLayout ws_layout(int n_seqs, int total_tokens, int H, int Dk, int Dv, bool kda
 struct WsPtrs {
   int *hdr, *chunk_seq, *chunk_tok, *chunk_len, *seq_chunk0, *seq_nch, *tail_start,
       *tail_len, *tail_pos, *order;
+  int *ready;  // per (chunk, head) tile: 1 once chunk prep has written it
   const float **state_ptrs;
   float *states;
   __nv_bfloat16 *T, *P, *W, *Qh, *Kt;
@@ -124,6 +127,7 @@ WsPtrs ws_ptrs(void *base, const WsLayout &w) {
   p.order = reinterpret_cast<int *>(b + w.order);
   p.state_ptrs = reinterpret_cast<const float **>(b + w.state_ptrs);
   p.states = reinterpret_cast<float *>(b + w.states);
+  p.ready = reinterpret_cast<int *>(b + w.ready);
   p.T = reinterpret_cast<__nv_bfloat16 *>(b + w.T);
   p.P = reinterpret_cast<__nv_bfloat16 *>(b + w.P);
   p.W = reinterpret_cast<__nv_bfloat16 *>(b + w.W);
@@ -178,6 +182,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
 constexpr int WL_THREADS = 1024;
 
 // One block. Validates cu_seqlens (cu[0] = 0, non-decreasing, cu[N] = Ntok);
+// hdr[0] = chunks in use, hdr[1] = chunk prep's tile counter (zeroed here);
 // on failure every sequence gets zero chunks and zero tail tokens, and the
 // error word is set. Otherwise sequence s gets Lc_s = max(L_s - K, 0) chunked
 // tokens in ceil(Lc_s / 64) chunks and a tail of L_s - Lc_s tokens, and the
@@ -185,10 +190,14 @@ constexpr int WL_THREADS = 1024;
 __global__ void __launch_bounds__(WL_THREADS)
     worklist_kernel(const int32_t *__restrict__ cu, int N, int total, int K, int H,
                     long long state_elems, const float *const *state_in, WsPtrs w,
-                    int *err) {
+                    long long n_ready, int *err) {
   __shared__ int bad;
   __shared__ int part[WL_THREADS];
   const int tid = threadIdx.x;
+  // chunk prep's tile counter, and the per-tile ready flags when the scan
+  // runs beside the prep
+  if (tid == 0) w.hdr[1] = 0;
+  for (long long e = tid; e < n_ready; e += WL_THREADS) w.ready[e] = 0;
   if (tid == 0) bad = (cu[0] != 0 || cu[N] != total) ? 1 : 0;
   __syncthreads();
   for (int s = tid; s < N; s += WL_THREADS)
@@ -308,13 +317,10 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
                       const float *__restrict__ beta, int H, int Hqk, int qk_grouped,
-                      WsPtrs w, int *err) {
+                      WsPtrs w, int publish, int *err) {
   constexpr int DK = 128;
-  const int c = blockIdx.x / H, h = blockIdx.x % H;
-  const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
-  if (c >= w.hdr[0]) return;
-  const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
-  const long long tile = (long long)c * H + h;
+  const int ntiles = w.hdr[0] * H;  // (chunks in use) x heads, chunk-major
+  if ((int)blockIdx.x >= ntiles) return;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   unsigned char *KQ = sm + PREP_KQ, *KB = sm + PREP_KB, *TZ = sm + PREP_TZ;
@@ -334,6 +340,17 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // K and Q rows of tile tl into KQ, completing on bar_tma (one thread)
+  auto load_tile = [&](int tl) {
+    const int lc = tl / H, lh = tl % H;
+    const int lq = qk_grouped ? lh / (H / Hqk) : lh % Hqk;
+    const int lt = w.chunk_tok[lc];
+    mbar_arrive_expect_tx(bar_tma, 32768);
+    tma_load_3d(KQ, &map_k, 0, lq, lt, bar_tma);
+    tma_load_3d(KQ + 16384, &map_k, 64, lq, lt, bar_tma);
+    tma_load_3d(KQ + 8192, &map_q, 0, lq, lt, bar_tma);
+    tma_load_3d(KQ + 16384 + 8192, &map_q, 64, lq, lt, bar_tma);
+  };
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(bar_tma, 1);
@@ -341,14 +358,34 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     mbar_init(bar_w, 1);
     fence_mbar_init();
   }
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_tma, 32768);
-    tma_load_3d(KQ, &map_k, 0, hq, t0, bar_tma);
-    tma_load_3d(KQ + 16384, &map_k, 64, hq, t0, bar_tma);
-    tma_load_3d(KQ + 8192, &map_q, 0, hq, t0, bar_tma);
-    tma_load_3d(KQ + 16384 + 8192, &map_q, 64, hq, t0, bar_tma);
+  if (warp == 0) {
+    tmem_alloc(tslot, 128);
+    tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  // Persistent: every CTA takes the next unclaimed tile (tiles go in chunk
+  // order) from the counter in hdr[1]; the copies of its next tile are issued
+  // as soon as the current one's last product has read K and Q. Thread 0
+  // claims, and counts the loads issued and waited for.
+  __shared__ int next_tile;
+  int loads_issued = 0, loads_done = 0;
+  if (tid == 0) {
+    const int t = atomicAdd(&w.hdr[1], 1);
+    next_tile = t;
+    if (t < ntiles) {
+      load_tile(t);
+      loads_issued = 1;
+    }
+  }
+  __syncthreads();
+  for (int it = 0, tl = next_tile; tl < ntiles; ++it) {
+  const uint32_t par = (uint32_t)(it & 1);
+  const int c = tl / H, h = tl % H;
+  const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
+  const long long tile = tl;
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
   // KDA gates, loaded while the tiles are in flight: thread = 8 channels
   // (column chunk kc) x 4 consecutive rows (row group krg); the 16 row groups
@@ -408,7 +445,10 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       smin[tid] = mn;
     }
   }
-  if (tid == 0 && !mbar_wait(bar_tma, 0, err, kSitePrepLoad)) abort_flag = 1;
+  if (tid == 0) {
+    if (mbar_wait(bar_tma, par, err, kSitePrepLoad)) ++loads_done;
+    else abort_flag = 1;
+  }
   __syncthreads();
   if constexpr (!KDA) {
     if (tid >= 32 && tid < CH) {
@@ -417,7 +457,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       slast[tid] = max(slast[tid], slast[31]);
     }
   }
-  if (abort_flag) return;
+  if (abort_flag) break;
   if (len < CH) {  // padding rows of K and Q are zero
     const int nz = (CH - len) * 8;
     for (int e = tid; e < nz * 2; e += PREP_THREADS) {
@@ -537,14 +577,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     stf[tid] = f;
   }
   fence_proxy_async();
-  if (warp == 0) {
-    tmem_alloc(tslot, 128);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
   if constexpr (!KDA) {
     // Decay from row j to row r: e^(gamma_r - gamma_j) = e^(gamma_r - m) e^(m - gamma_j)
     // with m the middle of the chunk's gate range. When that range is at most
@@ -571,7 +604,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_G, sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u),
                 sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u), idesc, s > 0);
     umma_commit(bar_g);
-    if (!mbar_wait(bar_g, 0, err, kSitePrepG)) abort_flag = 1;
+    if (!mbar_wait(bar_g, par, err, kSitePrepG)) abort_flag = 1;
   }
   __syncthreads();
   tc_fence_after();
@@ -648,10 +681,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   }
   tc_fence_before();
   __syncthreads();
-  if (abort_flag) {
-    if (warp == 0) tmem_dealloc(tbase, 128);
-    return;
-  }
+  if (abort_flag) break;
 
   // X = (I + A)^-1 by 16 x 16 blocks (A strictly lower triangular):
   //   X[R][R] = (I + A[R][R])^-1,
@@ -775,7 +805,16 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_W, sdesc_kmajor(smem_u32(TZ) + s * 32),
                 sdesc_mnmajor(smem_u32(KQ) + s * 2048, 16384), idesc, s > 0);
     umma_commit(bar_w);
-    if (!mbar_wait(bar_w, 0, err, kSitePrepW)) abort_flag = 1;
+    if (!mbar_wait(bar_w, par, err, kSitePrepW)) {
+      abort_flag = 1;
+    } else {  // K and Q are free: claim the next tile and issue its copies
+      const int t = atomicAdd(&w.hdr[1], 1);
+      next_tile = t;
+      if (t < ntiles) {
+        load_tile(t);
+        ++loads_issued;
+      }
+    }
   }
   __syncthreads();
   tc_fence_after();
@@ -792,6 +831,21 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       for (int q = 0; q < 4; ++q) dst[4 * q32 + q] = pack8(v + 8 * q);
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (abort_flag) break;
+  if (publish && tid == 0) {
+    // every thread's stores of this tile precede the barrier above; the
+    // release makes them visible before the flag (the scan acquires it)
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(w.ready + tile), "r"(1) : "memory");
+  }
+  tl = next_tile;
+  }  // tiles
+  // after an abort, copies still in flight land before the CTA exits
+  if (tid == 0 && loads_issued > loads_done)
+    mbar_wait(bar_tma, (uint32_t)(loads_done & 1), nullptr);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, 128);
@@ -895,6 +949,33 @@ __device__ __forceinline__ bool wait_ab(uint64_t *bar, uint32_t parity,
   return false;
 }
 
+// Wait of at most kReadyWaitNs for a tile's ready flag (set by chunk prep
+// with a release); then orders the async-proxy (TMA) reads of that tile after
+// the acquire. On a timeout the error word records the site and chunk.
+constexpr unsigned long long kReadyWaitNs = 2000000000ull;
+__device__ __forceinline__ bool wait_ready_flag(const int *flag, volatile int *abort_flag,
+                                                int *err, int jc) {
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return !*abort_flag;
+    }
+    if ((i & 255u) == 255u) {
+      if (*abort_flag) return false;
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > kReadyWaitNs) break;
+    }
+  }
+  set_error(err, kDevTimeout | (kSiteScanReady << 8) | ((jc & 0x7fff) << 16));
+  *abort_flag = 1;
+  return false;
+}
+
 // Wait used only while shutting down: bounded, ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   for (uint32_t i = 0; i < kDrainPolls; ++i)
@@ -931,8 +1012,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_out,
                       const float *const *state_in, float *__restrict__ out, int H,
                       int Hqk, int qk_grouped, float scale, WsPtrs w, float *ckpt,
-                      int ckpt_every, int max_ckpts, int *err) {
+                      int ckpt_every, int max_ckpts, int wait_ready, int *err) {
   constexpr int DK = 128, DV = 128;
+  // With wait_ready the chunk prep runs beside this kernel, launched after it
+  // as a programmatic dependent: it may start once every block of this grid
+  // has started, and this grid waits for its tiles through their ready flags.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
   const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
@@ -1001,6 +1086,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       const int gc = chunk0 + jc;
       const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
       const int trow = (gc * H + h) * CH;
+      if (wait_ready) {  // the tiles of chunk gc, head h are written
+        int ok = 1;
+        if (lane == 0) ok = wait_ready_flag(w.ready + gc * H + h, abort_flag, err, jc);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       if (lane == 0) {
         uint64_t *fb = &full[st];
         mbar_arrive_expect_tx(fb, ST_TX);
@@ -1394,20 +1484,32 @@ bool map_out_f32(CUtensorMap *m, void *base, int ntok, int H, int D) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opt-in shared-memory sizes, once per device.
+// Opt-in shared-memory sizes and the SM count, once per device.
 std::mutex g_attr_mu;
 bool g_attr_done[64] = {};
+int g_num_sms[64] = {};
 
-cudaError_t set_attributes() {
+cudaError_t set_attributes(int *num_sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_attr_mu);
-  if (dev >= 0 && dev < 64 && g_attr_done[dev]) return cudaSuccess;
+  if (g_attr_done[dev]) {
+    *num_sms = g_num_sms[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *num_sms = g_num_sms[dev];
   const void *fns[] = {(const void *)chunk_prep_kernel<false>,
                        (const void *)chunk_prep_kernel<true>};
   for (const void *f : fns) {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    // the whole unified L1 as shared memory, so that four CTAs fit per SM
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
   }
   const void *sfns[] = {(const void *)chunk_scan_kernel<false, false>,
@@ -1418,7 +1520,7 @@ cudaError_t set_attributes() {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
     if (e != cudaSuccess) return e;
   }
-  if (dev >= 0 && dev < 64) g_attr_done[dev] = true;
+  g_attr_done[dev] = true;
   return cudaSuccess;
 }
 
@@ -1443,7 +1545,7 @@ static cudaError_t launch_token_loop(const ChunkedArgs &a, cudaStream_t stream) 
   if (a.workspace_bytes < lay.total) return cudaErrorInvalidValue;
   const WsPtrs w = ws_ptrs(a.workspace, lay);
   worklist_kernel<<<1, WL_THREADS, 0, stream>>>(a.cu_seqlens, a.n_seqs, a.total_tokens,
-                                                0x7fffffff, a.H, 0, a.state_in, w, a.err);
+                                                0x7fffffff, a.H, 0, a.state_in, w, 0, a.err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   RecurrentArgs r{};
@@ -1461,7 +1563,8 @@ static cudaError_t launch_token_loop(const ChunkedArgs &a, cudaStream_t stream) 
 cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if (!tensor_core_route(a.bf16, a.Dk, a.Dv)) return launch_token_loop(a, stream);
   if (!encode_fn()) return cudaErrorNotSupported;
-  cudaError_t e = set_attributes();
+  int num_sms = 0;
+  cudaError_t e = set_attributes(&num_sms);
   if (e != cudaSuccess) return e;
   const WsLayout lay = ws_layout(a.n_seqs, a.total_tokens, a.H, a.Dk, a.Dv, a.kda);
   if (a.workspace_bytes < lay.total) return cudaErrorInvalidValue;
@@ -1470,7 +1573,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
 
   worklist_kernel<<<1, WL_THREADS, 0, stream>>>(a.cu_seqlens, a.n_seqs, a.total_tokens,
                                                 a.n_slots, a.H, state_elems, a.state_in, w,
-                                                a.err);
+                                                lay.max_chunks * a.H, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (a.total_tokens > 0) {
@@ -1487,32 +1590,57 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     if (a.kda && (!map_rows(&mQh, w.Qh, trows, a.Dk) || !map_rows(&mKt, w.Kt, trows, a.Dk)))
       return cudaErrorInvalidValue;
-    const long long prep_grid = lay.max_chunks * a.H;
-    if (a.kda)
-      chunk_prep_kernel<true><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          mq, mk, a.g, a.beta, a.H, Hqk, a.qk_grouped ? 1 : 0, w, a.err);
-    else
-      chunk_prep_kernel<false><<<(unsigned)prep_grid, PREP_THREADS, PREP_SMEM, stream>>>(
-          mq, mk, a.g, a.beta, a.H, Hqk, a.qk_grouped ? 1 : 0, w, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const unsigned scan_grid = (unsigned)((long long)a.n_seqs * a.H * 2);
     const int qg = a.qk_grouped ? 1 : 0;
-    if (a.kda && a.ckpt)
-      chunk_scan_kernel<true, true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
-          a.ckpt_every, a.max_ckpts, a.err);
-    else if (a.kda)
-      chunk_scan_kernel<true, false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr,
-          1, 0, a.err);
-    else if (a.ckpt)
-      chunk_scan_kernel<false, true><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
-          a.ckpt_every, a.max_ckpts, a.err);
-    else
-      chunk_scan_kernel<false, false><<<scan_grid, SCAN_THREADS, SCAN_SMEM, stream>>>(
-          mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr, 1,
-          0, a.err);
+    // persistent prep CTAs: as many as fit at once (registers allow three per
+    // SM for per-row gates, four for scalar gates; four use all of TMEM)
+    const int per_sm = a.kda ? 3 : 4;
+    auto launch_prep = [&](long long grid, bool pdl, int publish) -> cudaError_t {
+      const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H, grid));
+      if (a.kda)
+        return pdl ? launch_pdl(chunk_prep_kernel<true>, g3, dim3(PREP_THREADS), PREP_SMEM, stream,
+                                mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err)
+                   : (chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
+                          mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err),
+                      cudaGetLastError());
+      return pdl ? launch_pdl(chunk_prep_kernel<false>, g3, dim3(PREP_THREADS), PREP_SMEM, stream,
+                              mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err)
+                 : (chunk_prep_kernel<false><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
+                        mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err),
+                    cudaGetLastError());
+    };
+    const long long scan_grid = (long long)a.n_seqs * a.H * 2;
+    auto launch_scan = [&](int wait_ready) -> cudaError_t {
+      const unsigned sg = (unsigned)scan_grid;
+      if (a.kda && a.ckpt)
+        chunk_scan_kernel<true, true><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
+            mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+            a.ckpt_every, a.max_ckpts, wait_ready, a.err);
+      else if (a.kda)
+        chunk_scan_kernel<true, false><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
+            mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr,
+            1, 0, wait_ready, a.err);
+      else if (a.ckpt)
+        chunk_scan_kernel<false, true><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
+            mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+            a.ckpt_every, a.max_ckpts, wait_ready, a.err);
+      else
+        chunk_scan_kernel<false, false><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
+            mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr, 1,
+            0, wait_ready, a.err);
+      return cudaGetLastError();
+    };
+    // When the scan (one CTA per SM) leaves at least an eighth of the SMs
+    // free, it runs first and the prep beside it on the free SMs: the prep is
+    // a programmatic dependent of the scan, so every scan CTA is resident
+    // before any prep CTA starts, the prep never waits on the scan, and the
+    // scan waits for each tile's ready flag. Otherwise the prep runs first.
+    if (scan_grid <= num_sms - std::max(16, num_sms / 8)) {
+      if ((e = launch_scan(1)) != cudaSuccess) return e;
+      if ((e = launch_prep((num_sms - scan_grid) * per_sm, true, 1)) != cudaSuccess) return e;
+    } else {
+      if ((e = launch_prep((long long)num_sms * per_sm, false, 0)) != cudaSuccess) return e;
+      if ((e = launch_scan(0)) != cudaSuccess) return e;
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 

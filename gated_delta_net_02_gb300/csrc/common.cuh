@@ -30,6 +30,7 @@ enum WaitSite : int {
   kSiteScanO = 34,        // chunk scan, state warps: output product
   kSiteScanEmpty = 41,    // chunk scan, producer: a stage released by its products
   kSiteScanPad = 42,      // chunk scan, producer: copies of a partial last chunk
+  kSiteScanReady = 43,    // chunk scan, producer: a tile of the chunk prep running beside it
   kSiteScanStage = 52,    // chunk scan, MMA issuer: a stage's copies
   kSiteScanS0 = 53,       // chunk scan, MMA issuer: the state operand
   kSiteScanD = 54,        // chunk scan, MMA issuer: the D tile
