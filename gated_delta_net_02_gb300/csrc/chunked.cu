@@ -302,12 +302,15 @@ static_assert(PREP_TZ % 1024 == 0 && PREP_KB % 1024 == 0, "swizzled atoms are 10
 static_assert(64 * XS_LD * 4 >= 16384, "X region also holds KB");
 
 // Byte offset of A(r, j) (fp32) inside KQ once G is done: rows 0..31 in the
-// Q rows of half 0, rows 32..63 in those of half 1; 64 floats per row with
-// the column XOR-ed by (r & 15), so that 32 threads writing one column of
-// 32 consecutive rows hit 16 different banks, and the swizzle of a row
-// depends only on r mod 16.
+// Q rows of half 0, rows 32..63 in those of half 1; 64 floats (16 pieces of
+// 16 bytes) per row with the piece index XOR-ed by (r & 15): a thread
+// writes 4 consecutive columns of its row as one 16-byte store, 32 threads
+// storing the same columns of 32 consecutive rows take the minimum 4
+// wavefronts, and the tensor-core fragment reads of the solve (rows g, g+8,
+// columns t, t+4 of a 16 x 8 tile) touch 32 different banks.
 __device__ __forceinline__ uint32_t af_off(int r, int j) {
-  return (uint32_t)((r >> 5) * 16384 + 8192 + (r & 31) * 256 + ((j ^ (r & 15)) << 2));
+  return (uint32_t)((r >> 5) * 16384 + 8192 + (r & 31) * 256 + ((((j >> 2) ^ (r & 15))) << 4) +
+                    ((j & 3) << 2));
 }
 
 // One CTA per (chunk, head). Rows r of the chunk are tokens chunk_tok + r,
@@ -629,16 +632,25 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
             a = br * G[u];
             if constexpr (!KDA) a *= __expf(gr - sgam[j]);
           }
-          *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
+          G[u] = a;
         }
+        unsigned char *arow = KQ + af_off(r, 0) - ((r & 15) << 4);  // row base
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          *reinterpret_cast<float4 *>(arow + ((((j0 >> 2) + c4) ^ (r & 15)) << 4)) =
+              make_float4(G[4 * c4], G[4 * c4 + 1], G[4 * c4 + 2], G[4 * c4 + 3]);
       } else {
         const float brf = br * srowf[r];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int j = j0 + u;
-          const float a = j < r && j >= lr ? brf * G[u] * scolf[j] : 0.f;
-          *reinterpret_cast<float *>(KQ + af_off(r, j)) = a;
+          G[u] = j < r && j >= lr ? brf * G[u] * scolf[j] : 0.f;
         }
+        unsigned char *arow = KQ + af_off(r, 0) - ((r & 15) << 4);  // row base
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          *reinterpret_cast<float4 *>(arow + ((((j0 >> 2) + c4) ^ (r & 15)) << 4)) =
+              make_float4(G[4 * c4], G[4 * c4 + 1], G[4 * c4 + 2], G[4 * c4 + 3]);
       }
     } else {
       const int r = row - CH;
@@ -694,17 +706,25 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   {
     if (tid < CH) {  // diagonal block R, column c: right-looking substitution
       const int R = tid >> 4, c = tid & 15, r0 = 16 * R;
+      // A(r0 + u2, r0 + u) sits at ablk[u2 >> 2] + 256 u2 + 16 ((u >> 2) ^ (u2 & 3))
+      // + 4 (u & 3): four bases per thread, the rest compile-time offsets
+      const unsigned char *arow = KQ + (R >> 1) * 16384 + 8192 + (R & 1) * 4096;
+      const unsigned char *ablk[4] = {arow + 64 * (R ^ 0), arow + 64 * (R ^ 1),
+                                      arow + 64 * (R ^ 2), arow + 64 * (R ^ 3)};
+      float *xcol = Xs + r0 * XS_LD + r0 + c;
       float acc[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) acc[u] = 0.f;
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const float xu = (u == c ? 1.f : 0.f) - acc[u];
-        Xs[(r0 + u) * XS_LD + r0 + c] = xu;
+        xcol[u * XS_LD] = xu;
 #pragma unroll
         for (int u2 = u + 1; u2 < 16; ++u2)
-          acc[u2] = fmaf(*reinterpret_cast<const float *>(KQ + af_off(r0 + u2, r0 + u)), xu,
-                         acc[u2]);
+          acc[u2] = fmaf(*reinterpret_cast<const float *>(ablk[u2 >> 2] + 256 * u2 +
+                                                          16 * ((u >> 2) ^ (u2 & 3)) +
+                                                          4 * (u & 3)),
+                         xu, acc[u2]);
       }
     } else {  // zero blocks above the diagonal
       for (int e = tid - CH; e < 6 * 256; e += PREP_THREADS - CH) {

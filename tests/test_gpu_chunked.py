@@ -231,3 +231,25 @@ def test_kda_precision_margin(gdn, T, seed):
     w_st, at_st = worst_head(slots[:, -1].double().cpu().numpy(), s_ref)
     print(f"KDA T={T} seed={seed}: out {e_out:.3e} (worst head {w_out:.3e} at {at_out}), "
           f"state {e_fin:.3e} (worst head {w_st:.3e} at {at_st})")
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
+def test_prep_beside_scan_equals_prep_before_scan(gdn, mode):
+    """A batch of 8 sequences x 16 heads needs 256 scan CTAs, more than the SMs,
+    so chunk prep runs before the scan; one sequence alone (32 scan CTAs) runs
+    the prep beside the scan on the free SMs, the scan waiting for each tile's
+    ready flag. Per tile and per chain the arithmetic is the same, so every
+    sequence's outputs and slots must agree bit for bit between the two."""
+    lens = [200, 330, 64, 129, 257, 70, 300, 191]
+    b = inputs.make_batch(250, lens, 16, 128, 128, mode=mode, n_slots=3)
+    assert torch.cuda.get_device_properties(0).multi_processor_count < 256
+    out_all, slots_all = chunked_forward(gdn, b)
+    cu = b.cu_seqlens.tolist()
+    for s in range(len(lens)):
+        sl = slice(cu[s], cu[s + 1])
+        one = inputs.GDNBatch(b.q[sl], b.k[sl], b.v[sl], b.g[sl], b.beta[sl],
+                              b.state[s:s + 1], mode, b.scale, torch.tensor([lens[s]]), 3)
+        out_one, slots_one = chunked_forward(gdn, one)
+        assert torch.equal(out_one, out_all[sl]), f"sequence {s}"
+        assert torch.equal(slots_one[0], slots_all[s]), f"sequence {s}"
+    compare(b, out_all, slots_all)
