@@ -343,11 +343,11 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // K and Q rows of tile tl into KQ, completing on bar_tma (one thread)
-  auto load_tile = [&](int tl) {
-    const int lc = tl / H, lh = tl % H;
+  // K and Q rows of tile tl (first token lt) into KQ, completing on bar_tma
+  // (one thread)
+  auto load_tile = [&](int tl, int lt) {
+    const int lh = tl % H;
     const int lq = qk_grouped ? lh / (H / Hqk) : lh % Hqk;
-    const int lt = w.chunk_tok[lc];
     mbar_arrive_expect_tx(bar_tma, 32768);
     tma_load_3d(KQ, &map_k, 0, lq, lt, bar_tma);
     tma_load_3d(KQ + 16384, &map_k, 64, lq, lt, bar_tma);
@@ -373,13 +373,13 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   // order) from the counter in hdr[1]; the copies of its next tile are issued
   // as soon as the current one's last product has read K and Q. Thread 0
   // claims, and counts the loads issued and waited for.
-  __shared__ int next_tile;
+  __shared__ int next_tile, s_claim[2];
   int loads_issued = 0, loads_done = 0;
   if (tid == 0) {
     const int t = atomicAdd(&w.hdr[1], 1);
     next_tile = t;
     if (t < ntiles) {
-      load_tile(t);
+      load_tile(t, w.chunk_tok[t / H]);
       loads_issued = 1;
     }
   }
@@ -448,9 +448,13 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       smin[tid] = mn;
     }
   }
+  // thread 0: the tile after this one and its first token, claimed and read
+  // early so that the atomic's and the load's latencies hide behind this tile
+  // (kept in shared memory: no registers live across the tile)
   if (tid == 0) {
     if (mbar_wait(bar_tma, par, err, kSitePrepLoad)) ++loads_done;
     else abort_flag = 1;
+    s_claim[0] = atomicAdd(&w.hdr[1], 1);
   }
   __syncthreads();
   if constexpr (!KDA) {
@@ -607,6 +611,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_G, sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u),
                 sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u), idesc, s > 0);
     umma_commit(bar_g);
+    if (s_claim[0] < ntiles) s_claim[1] = w.chunk_tok[s_claim[0] / H];
     if (!mbar_wait(bar_g, par, err, kSitePrepG)) abort_flag = 1;
   }
   __syncthreads();
@@ -827,11 +832,10 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     umma_commit(bar_w);
     if (!mbar_wait(bar_w, par, err, kSitePrepW)) {
       abort_flag = 1;
-    } else {  // K and Q are free: claim the next tile and issue its copies
-      const int t = atomicAdd(&w.hdr[1], 1);
-      next_tile = t;
-      if (t < ntiles) {
-        load_tile(t);
+    } else {  // K and Q are free: the next tile's copies
+      next_tile = s_claim[0];
+      if (s_claim[0] < ntiles) {
+        load_tile(s_claim[0], s_claim[1]);
         ++loads_issued;
       }
     }
