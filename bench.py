@@ -191,12 +191,17 @@ def timed_graph_steps(graphs, K, stream):
     return start.elapsed_time(end)
 
 
-def capture(fn_steps, stream, steps):
-    """CUDA graph of `steps` consecutive calls fn_steps(i) for i in steps."""
+def capture(fn_steps, stream, steps, pre=None, post=None):
+    """CUDA graph of `steps` consecutive calls fn_steps(i) for i in steps
+    (with pre() before and post() after them, inside the capture)."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        if pre:
+            pre()
         for i in steps:
             fn_steps(i)
+        if post:
+            post()
     return g
 
 
@@ -205,8 +210,9 @@ def capture(fn_steps, stream, steps):
 class PackedInputs:
     """End-to-end staging: a step's host inputs (q, k, v, g, beta) packed at
     256-byte offsets in one pinned buffer per step, copied with one
-    host-to-device copy into a device buffer of the same layout, whose typed
-    views are what the API call receives."""
+    host-to-device copy into one of two device buffers of the same layout
+    (double-buffered, so that the next step's copy can run during this step),
+    whose typed views are what the API call receives."""
 
     def __init__(self, host, dev):
         # host: tensors with a leading step dimension [P, ...] (P may be 1)
@@ -222,13 +228,63 @@ class PackedInputs:
         self.host = torch.zeros(P, off, dtype=torch.uint8).pin_memory()
         for t, o, nb in zip(host, self.offs, self.nbytes):
             self.host[:, o:o + nb].copy_(t.reshape(P, -1).view(torch.uint8))
-        self.stage = torch.empty(off, dtype=torch.uint8, device=dev)
-        self.views = [self.stage[o:o + nb].view(t.dtype).view(t.shape[1:])
-                      for t, o, nb in zip(host, self.offs, self.nbytes)]
+        self.stage = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.views = [[st[o:o + nb].view(t.dtype).view(t.shape[1:])
+                       for t, o, nb in zip(host, self.offs, self.nbytes)] for st in self.stage]
 
-    def copy_in(self, p):
-        self.stage.copy_(self.host[p], non_blocking=True)
-        return self.views
+    def copy_in(self, p, b):
+        """Host step p into device buffer b (on the current stream)."""
+        self.stage[b].copy_(self.host[p], non_blocking=True)
+        return self.views[b]
+
+
+class E2EPipeline:
+    """End-to-end steps with the copies of neighbouring steps overlapping:
+    step i's inputs go host -> device buffer i % 2 on a copy-in stream, the
+    API call runs on the launch stream once they have landed (and once the
+    output buffer i % 2 has been read back by step i - 2), and step i's output
+    goes device -> pinned host on a copy-out stream after the call. Every
+    step's two copies stay inside the timed region; captured into the same
+    CUDA graph as the calls (event edges between the three streams)."""
+
+    def __init__(self, wl, dev):
+        self.wl = wl
+        self.cs_in = torch.cuda.Stream(device=dev)
+        self.cs_out = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def begin(self, stream):
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.cs_in.wait_event(ev)
+        self.cs_out.wait_event(ev)
+        self.used = [False, False]
+
+    def step(self, i, stream):
+        wl, b = self.wl, i % 2
+        with torch.cuda.stream(self.cs_in):
+            if self.used[b]:   # buffer b was last read by the call of step i - 2
+                self.cs_in.wait_event(self.ev_done[b])
+            views = wl.packed.copy_in(wl.e2e_host_index(i), b)
+            self.ev_in[b].record(self.cs_in)
+        stream.wait_event(self.ev_in[b])
+        if self.used[b]:       # output b of step i - 2 has been read back
+            stream.wait_event(self.ev_out[b])
+        wl.e2e_call(i, views, wl.out2[b], stream)
+        self.ev_done[b].record(stream)
+        with torch.cuda.stream(self.cs_out):
+            self.cs_out.wait_event(self.ev_done[b])
+            wl.out_host2[b].copy_(wl.out2[b], non_blocking=True)
+            self.ev_out[b].record(self.cs_out)
+        self.used[b] = True
+
+    def end(self, stream):
+        for b in range(2):
+            if self.used[b]:
+                stream.wait_event(self.ev_out[b])
+                stream.wait_event(self.ev_in[b])
 
 
 class Decode:
@@ -281,7 +337,9 @@ class Decode:
         self.shape = gdn.gdn_shape(N, 1, H, D, D, gdn.GDN_BF16, D ** -0.5)
         # e2e: packed pinned host pool, one device staging buffer, pinned output
         self.packed = PackedInputs(self.host, dev)
-        self.out_host = torch.empty(N, H, D, dtype=torch.float32).pin_memory()
+        self.out2 = [self.out, torch.empty_like(self.out)]
+        self.out_host2 = [torch.empty(N, H, D, dtype=torch.float32).pin_memory()
+                          for _ in range(2)]
         self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
@@ -299,12 +357,13 @@ class Decode:
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, self.out, 1, "gda",
                              stream)
 
-    def step_e2e(self, i, stream):
-        q, k, v, g, beta = self.packed.copy_in(i % self.POOL)
+    def e2e_host_index(self, i):
+        return i % self.POOL
+
+    def e2e_call(self, i, views, out, stream):
+        q, k, v, g, beta = views
         src, dst = self._bufs(i)
-        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, self.out, 1, "gda",
-                             stream)
-        self.out_host.copy_(self.out, non_blocking=True)
+        self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, out, 1, "gda", stream)
 
     def graph_len(self):
         return self.POOL  # a multiple of 2 x SETS: replays continue every chain
@@ -380,7 +439,9 @@ class Verify(Decode):
         self.out = torch.empty(N * T, H, D, device=dev)
         self.shape = gdn.gdn_shape(N, T, H, D, D, gdn.GDN_BF16, D ** -0.5)
         self.packed = PackedInputs(self.host, dev)
-        self.out_host = torch.empty(N * T, H, D, dtype=torch.float32).pin_memory()
+        self.out2 = [self.out, torch.empty_like(self.out)]
+        self.out_host2 = [torch.empty(N * T, H, D, dtype=torch.float32).pin_memory()
+                          for _ in range(2)]
         self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
@@ -390,11 +451,10 @@ class Verify(Decode):
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
                              self.slots, self.out, self.K, "gda", stream)
 
-    def step_e2e(self, i, stream):
-        q, k, v, g, beta = self.packed.copy_in(i % self.POOL)
+    def e2e_call(self, i, views, out, stream):
+        q, k, v, g, beta = views
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
-                             self.slots, self.out, self.K, "gda", stream)
-        self.out_host.copy_(self.out, non_blocking=True)
+                             self.slots, out, self.K, "gda", stream)
 
     def graph_len(self):
         return self.POOL
@@ -443,7 +503,8 @@ class Prefill:
         self.out = torch.empty(self.ntok, self.H, 128, device=dev)
         self.packed = PackedInputs([getattr(b0, n).unsqueeze(0)
                                     for n in ("q", "k", "v", "g", "beta")], dev)
-        self.out_host = torch.empty(self.ntok, self.H, 128).pin_memory()
+        self.out2 = [self.out, torch.empty_like(self.out)]
+        self.out_host2 = [torch.empty(self.ntok, self.H, 128).pin_memory() for _ in range(2)]
         self.h2d_bytes = self.packed.step_bytes
         self.d2h_bytes = self.out.numel() * 4
 
@@ -470,20 +531,22 @@ class Prefill:
         C, D = 64, 128
         return (2 * C * (3 * D + 2 * D) + 6 * D * D) * self.ntok * self.H
 
-    def _call(self, d, q, k, v, g, beta, stream):
+    def _call(self, d, q, k, v, g, beta, stream, out=None):
         self.gdn.gdn_forward_chunked(self.shape, d["cu"], q, k, v, g, beta, d["ptrs"],
-                                     self.slots, self.out, self.K, self.mode, self.ws,
-                                     self.ws_bytes, stream)
+                                     self.slots, self.out if out is None else out, self.K,
+                                     self.mode, self.ws, self.ws_bytes, stream)
 
     def step(self, i, stream):
         _, d = self.sets[i % self.SETS]
         self._call(d, d["q"], d["k"], d["v"], d["g"], d["beta"], stream)
 
-    def step_e2e(self, i, stream):
-        q, k, v, g, beta = self.packed.copy_in(0)
+    def e2e_host_index(self, i):
+        return 0
+
+    def e2e_call(self, i, views, out, stream):
+        q, k, v, g, beta = views
         _, d = self.sets[0]
-        self._call(d, q, k, v, g, beta, stream)
-        self.out_host.copy_(self.out, non_blocking=True)
+        self._call(d, q, k, v, g, beta, stream, out)
 
     def graph_len(self):
         return 4
@@ -626,10 +689,11 @@ class PrefillVarlenCkpt(PrefillVarlen):
     def alg_bytes_per_step(self):
         return super().alg_bytes_per_step() + self.n_ckpts() * self.H * 128 * 128 * 4
 
-    def _call(self, d, q, k, v, g, beta, stream):
+    def _call(self, d, q, k, v, g, beta, stream, out=None):
         self.gdn.gdn_forward_chunked_checkpointed(
-            self.shape, d["cu"], q, k, v, g, beta, d["ptrs"], self.slots, self.out, self.K,
-            self.mode, self.ckpts, self.EVERY, self.MAX_CKPTS, self.ws, self.ws_bytes, stream)
+            self.shape, d["cu"], q, k, v, g, beta, d["ptrs"], self.slots,
+            self.out if out is None else out, self.K, self.mode, self.ckpts, self.EVERY,
+            self.MAX_CKPTS, self.ws, self.ws_bytes, stream)
 
     def config(self):
         c = super().config()
@@ -736,13 +800,14 @@ def measure(wl, args, gdn, dev, stream, ws, rank, local):
     L = wl.graph_len()
     K, W = args.steps, args.warmup
 
-    def graphs_for(step_fn):
+    def graphs_for(step_fn, L=L, pre=None, post=None):
         gs = []
         with torch.cuda.stream(stream):
-            gs.append((capture(lambda i: step_fn(i, stream), stream, range(L)), L))
+            gs.append((capture(lambda i: step_fn(i, stream), stream, range(L), pre, post), L))
             rem = K % L
             if rem:
-                gs.append((capture(lambda i: step_fn(i, stream), stream, range(rem)), rem))
+                gs.append((capture(lambda i: step_fn(i, stream), stream, range(rem), pre, post),
+                           rem))
         return gs
 
     # warm-up: W eager steps (also initialises per-device state before capture)
@@ -769,8 +834,12 @@ def measure(wl, args, gdn, dev, stream, ws, rank, local):
     gdn.gdn_check_device_error(stream)
     del graphs
 
-    # e2e: host tokens in, host outputs back, per step, same K
-    graphs_e2e = graphs_for(wl.step_e2e)
+    # e2e: host inputs in, host outputs back, every step, same K; the copies
+    # of neighbouring steps overlap each call (E2EPipeline), within graphs of
+    # at least 16 steps
+    pipe = E2EPipeline(wl, dev)
+    graphs_e2e = graphs_for(pipe.step, max(L, min(K, 16)), lambda: pipe.begin(stream),
+                            lambda: pipe.end(stream))
     with torch.cuda.stream(stream):
         for g, _ in graphs_e2e:
             g.replay()
