@@ -1241,29 +1241,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       }
       for (int jc = 0; ok && jc < nch; ++jc) {
         const int st = jc & 1;
-        // wait for D(jc); issue the next chunk's state-free part as soon as
-        // its stage is usable, whichever comes first
-        bool x1_done = jc + 1 >= nch;
-        uint64_t *nb = x1_done ? nullptr : stage_bar(jc + 1, &par);
-        bool d_ready = false;
-        for (uint32_t it = 0; it < kMaxPolls; ++it) {
-          if (!x1_done && mbar_test_wait(nb, par)) {
-            issue_x1(jc + 1);
-            x1_done = true;
-          }
-          if (mbar_test_wait(bE6, jc & 1)) {
-            d_ready = true;
-            break;
-          }
-          if ((it & 1023u) == 1023u && *abort_flag) break;
-        }
-        if (!d_ready || *abort_flag) {
-          if (!d_ready && !*abort_flag) {
-            set_error(err, kDevTimeout | (kSiteScanD << 8) | ((jc & 0x7fff) << 16));
-            *abort_flag = 1;
-          }
-          break;
-        }
+        // D(jc) in shared memory (the next chunk's state-free product is issued
+        // only behind this chunk's S and O products, so that nothing stands
+        // between D(jc) and S(jc) in the in-order tensor pipe)
+        if (!wait_ab(bE6, jc & 1, abort_flag, err, kSiteScanD, jc)) break;
         tc_fence_after();
         // S_acc = K~^T D~
         const uint64_t dB = KDA ? dD[jc & 1] : dDT;
@@ -1279,10 +1260,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         umma_commit(&bE8[jc & 1]);
         umma_commit(&empty[st]);
         if (jc + 1 < nch) {
-          if (!x1_done) {
-            if (!wait_ab(nb, par, abort_flag, err, kSiteScanStage, jc + 1)) break;
-            issue_x1(jc + 1);
-          }
+          uint64_t *nb = stage_bar(jc + 1, &par);
+          if (!wait_ab(nb, par, abort_flag, err, kSiteScanStage, jc + 1)) break;
+          issue_x1(jc + 1);
           if (!issue_x2(jc + 1)) break;
         }
       }

@@ -93,20 +93,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of phase `parity` (try_wait may suspend the thread for a
-// while; this returns at once, for loops that poll several barriers).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for phase `parity` of `bar` to complete, polling at most max_polls
 // times. Returns false (and sets the error word, with `site` in bits 8..15)
 // if the wait ran out.
