@@ -320,10 +320,23 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const float *__restrict__ g,
                       const float *__restrict__ beta, int H, int Hqk, int qk_grouped,
-                      WsPtrs w, int publish, int *err) {
+                      WsPtrs w, int publish, int handoff_sms, int num_sms, int *err) {
   constexpr int DK = 128;
+  // A chunk scan launched after this grid as a programmatic dependent may
+  // start once every CTA here has started (hand-off mode, see below).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ntiles = w.hdr[0] * H;  // (chunks in use) x heads, chunk-major
   if ((int)blockIdx.x >= ntiles) return;
+  // Hand-off: the CTAs on about handoff_sms of the SMs take one tile each and
+  // leave, so that the scan's CTAs (one per SM) take those SMs while the rest
+  // of the prep goes on beside them.
+  bool one_tile = false;
+  if (handoff_sms > 0) {
+    uint32_t smid, nsmid;
+    asm("mov.u32 %0, %%smid;" : "=r"(smid));
+    asm("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
+    one_tile = (long long)smid * num_sms < (long long)handoff_sms * nsmid;
+  }
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   unsigned char *KQ = sm + PREP_KQ, *KB = sm + PREP_KB, *TZ = sm + PREP_TZ;
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   if (tid == 0) {
     if (mbar_wait(bar_tma, par, err, kSitePrepLoad)) ++loads_done;
     else abort_flag = 1;
-    s_claim[0] = atomicAdd(&w.hdr[1], 1);
+    s_claim[0] = one_tile ? ntiles : atomicAdd(&w.hdr[1], 1);
   }
   __syncthreads();
   if constexpr (!KDA) {
@@ -1038,10 +1051,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       int Hqk, int qk_grouped, float scale, WsPtrs w, float *ckpt,
                       int ckpt_every, int max_ckpts, int wait_ready, int *err) {
   constexpr int DK = 128, DV = 128;
-  // With wait_ready the chunk prep runs beside this kernel, launched after it
-  // as a programmatic dependent: it may start once every block of this grid
-  // has started, and this grid waits for its tiles through their ready flags.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // With wait_ready this grid is a programmatic dependent of the chunk prep,
+  // which is still running: the work list (an earlier kernel) is complete,
+  // and each chunk's tiles are read only after their ready flags (no
+  // griddepcontrol.wait, which would wait for the whole prep).
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
   const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
@@ -1598,53 +1611,67 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     // persistent prep CTAs: as many as fit at once (registers allow three per
     // SM for per-row gates, four for scalar gates; four use all of TMEM)
     const int per_sm = a.kda ? 3 : 4;
-    auto launch_prep = [&](long long grid, bool pdl, int publish) -> cudaError_t {
-      const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H, grid));
+    auto launch_prep = [&](int publish, int handoff) -> cudaError_t {
+      const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H,
+                                                  (long long)num_sms * per_sm));
       if (a.kda)
-        return pdl ? launch_pdl(chunk_prep_kernel<true>, g3, dim3(PREP_THREADS), PREP_SMEM, stream,
-                                mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err)
-                   : (chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
-                          mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err),
-                      cudaGetLastError());
-      return pdl ? launch_pdl(chunk_prep_kernel<false>, g3, dim3(PREP_THREADS), PREP_SMEM, stream,
-                              mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err)
-                 : (chunk_prep_kernel<false><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
-                        mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, a.err),
-                    cudaGetLastError());
+        chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
+            mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
+      else
+        chunk_prep_kernel<false><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
+            mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
+      return cudaGetLastError();
     };
     const long long scan_grid = (long long)a.n_seqs * a.H * 2;
     auto launch_scan = [&](int wait_ready) -> cudaError_t {
-      const unsigned sg = (unsigned)scan_grid;
+      const dim3 sg((unsigned)scan_grid), st(SCAN_THREADS);
+      const int ce = a.ckpt ? a.ckpt_every : 1, cm = a.ckpt ? a.max_ckpts : 0;
+      // as a programmatic dependent of the prep when it waits for ready flags
       if (a.kda && a.ckpt)
-        chunk_scan_kernel<true, true><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
-            mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
-            a.ckpt_every, a.max_ckpts, wait_ready, a.err);
-      else if (a.kda)
-        chunk_scan_kernel<true, false><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
-            mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr,
-            1, 0, wait_ready, a.err);
-      else if (a.ckpt)
-        chunk_scan_kernel<false, true><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
-            mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
-            a.ckpt_every, a.max_ckpts, wait_ready, a.err);
-      else
-        chunk_scan_kernel<false, false><<<sg, SCAN_THREADS, SCAN_SMEM, stream>>>(
-            mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, nullptr, 1,
-            0, wait_ready, a.err);
-      return cudaGetLastError();
+        return wait_ready ? launch_pdl(chunk_scan_kernel<true, true>, sg, st, SCAN_SMEM, stream,
+                                       mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
+                                       qg, a.scale, w, a.ckpt, ce, cm, wait_ready, a.err)
+                          : (chunk_scan_kernel<true, true><<<sg, st, SCAN_SMEM, stream>>>(
+                                 mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
+                                 a.scale, w, a.ckpt, ce, cm, wait_ready, a.err),
+                             cudaGetLastError());
+      if (a.kda)
+        return wait_ready ? launch_pdl(chunk_scan_kernel<true, false>, sg, st, SCAN_SMEM, stream,
+                                       mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
+                                       qg, a.scale, w, (float *)nullptr, ce, cm, wait_ready,
+                                       a.err)
+                          : (chunk_scan_kernel<true, false><<<sg, st, SCAN_SMEM, stream>>>(
+                                 mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
+                                 a.scale, w, nullptr, ce, cm, wait_ready, a.err),
+                             cudaGetLastError());
+      if (a.ckpt)
+        return wait_ready ? launch_pdl(chunk_scan_kernel<false, true>, sg, st, SCAN_SMEM, stream,
+                                       mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
+                                       qg, a.scale, w, a.ckpt, ce, cm, wait_ready, a.err)
+                          : (chunk_scan_kernel<false, true><<<sg, st, SCAN_SMEM, stream>>>(
+                                 mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
+                                 a.scale, w, a.ckpt, ce, cm, wait_ready, a.err),
+                             cudaGetLastError());
+      return wait_ready ? launch_pdl(chunk_scan_kernel<false, false>, sg, st, SCAN_SMEM, stream,
+                                     mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
+                                     a.scale, w, (float *)nullptr, ce, cm, wait_ready, a.err)
+                        : (chunk_scan_kernel<false, false><<<sg, st, SCAN_SMEM, stream>>>(
+                               mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
+                               a.scale, w, nullptr, ce, cm, wait_ready, a.err),
+                           cudaGetLastError());
     };
-    // When the scan (one CTA per SM) leaves at least an eighth of the SMs
-    // free, it runs first and the prep beside it on the free SMs: the prep is
-    // a programmatic dependent of the scan, so every scan CTA is resident
-    // before any prep CTA starts, the prep never waits on the scan, and the
-    // scan waits for each tile's ready flag. Otherwise the prep runs first.
-    if (scan_grid <= num_sms - std::max(16, num_sms / 8)) {
-      if ((e = launch_scan(1)) != cudaSuccess) return e;
-      if ((e = launch_prep((num_sms - scan_grid) * per_sm, true, 1)) != cudaSuccess) return e;
-    } else {
-      if ((e = launch_prep((long long)num_sms * per_sm, false, 0)) != cudaSuccess) return e;
-      if ((e = launch_scan(0)) != cudaSuccess) return e;
-    }
+    // The prep runs first, on every SM. When the scan (one CTA per SM)
+    // leaves at least an eighth of the SMs free, it is launched right behind
+    // the prep as a programmatic dependent ("hand-off"): the prep CTAs on as
+    // many SMs as the scan has CTAs take one tile each and leave, the scan's
+    // CTAs take those SMs and wait for each tile's ready flag while the rest
+    // of the prep goes on. The scan can start only once every prep CTA has
+    // started, and the prep never waits on the scan, so the prep always
+    // finishes. Otherwise the scan simply runs after the prep.
+    const bool handoff = scan_grid <= num_sms - std::max(16, num_sms / 8);
+    if ((e = launch_prep(handoff ? 1 : 0, handoff ? (int)scan_grid : 0)) != cudaSuccess)
+      return e;
+    if ((e = launch_scan(handoff ? 1 : 0)) != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 

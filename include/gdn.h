@@ -166,12 +166,14 @@ size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots);
  * workspace   device buffer of at least gdn_chunked_workspace_size bytes,
  *             256-byte aligned; its contents on entry do not matter.
  * Gate range: inside each 64-token chunk the cumulative log-gate from the
- * chunk's first token must stay within [-80, 80] for per-row gates (for
- * scalar gates only growth above e^80 is limited; any decay is exact). The
- * chunk form keeps its decay factors e^(+-gamma) in bf16/fp32, whose range
- * ends near e^88. A chunk outside it leaves its outputs undefined and makes
- * gdn_check_device_error return GDN_ERR_DEVICE_ARG; gdn_forward (the token
- * loop) has no such limit.
+ * chunk's first token must stay within [-80, 80] for per-row gates. For
+ * scalar gates only growth is limited (no interval of the chunk may grow by
+ * more than e^80); any decay is computed, and a gate of -inf resets the state
+ * exactly. The chunk form keeps its decay factors e^(+-gamma) in bf16/fp32,
+ * whose range ends near e^88. A chunk outside the range (a NaN gate too)
+ * leaves its outputs undefined and makes gdn_check_device_error return
+ * GDN_ERR_DEVICE_ARG; gdn_forward (the token loop) has no such limit, and
+ * the last n_slots tokens of each sequence, which run through it, neither.
  */
 gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
                                const int32_t *cu_seqlens, const void *q,
@@ -198,7 +200,10 @@ gdn_status gdn_forward_chunked(const gdn_varlen_shape *shape,
  *    fp32 state per (sequence, head): 1 x 4096 tokens x 32 heads needs about
  *    140 MB per-row and fits; 8 x ~4k tokens x 16 heads does not.
  *  - The first call on a device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current and keeps it for the life of the process; make that
+ *    first call before any stream capture. A cudaDeviceReset invalidates the
+ *    kept address (as it does the error word's): do not call this entry
+ *    point after resetting a device it was used on.
  *  - Every call on a device shares the one array and it keeps the previous
  *    call's contents; nothing in it needs to start at zero (the work list
  *    rewrites what the later kernels read). Calls that can overlap on the
