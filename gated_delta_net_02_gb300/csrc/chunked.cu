@@ -157,21 +157,25 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
   return u;
 }
 
-// tf32 high part of x (round to nearest) and the tf32 rounding of the rest:
-// x = hi + lo up to the last bits of lo.
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
+// bf16 high parts of (x0, x1) and the bf16 roundings of the rests, packed in
+// pairs (x0 in the low half): x = hi + lo to about 2^-16 relative.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Warp-level D (16 x 8, fp32) += A (16 x 8, tf32, row-major) * B (8 x 8, tf32),
-// fragments as the PTX ISA lays out mma.m16n8k8 (g = lane / 4, t = lane % 4):
-// a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
-// d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
+// Warp-level D (16 x 8, fp32) += A (16 x 16, bf16, row-major) * B (16 x 8,
+// bf16), fragments as the PTX ISA lays out mma.m16n8k16 (g = lane / 4,
+// t = lane % 4; each register a pair of consecutive K indices):
+// a = A[g][2t..], A[g+8][2t..], A[g][2t+8..], A[g+8][2t+8..];
+// b = B[2t..][g], B[2t+8..][g]; d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
@@ -718,9 +722,10 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   //   X[R][K] = -X[R][R] sum_{M=K..R-1} A[R][M] X[M][K]      (K < R),
   // one block row after another. The four diagonal inverses are forward
   // substitutions on the CUDA cores (thread = block and column); the block
-  // products run on the tensor cores as warp-level tf32 MMAs with every
-  // operand split into a tf32 high and low part (hi*hi + hi*lo + lo*hi), which
-  // keeps them at fp32 accuracy. X goes to Xs (fp32, row stride XS_LD).
+  // products run on the tensor cores as warp-level bf16 MMAs with every
+  // operand split into a bf16 high and low part (hi*hi + hi*lo + lo*hi),
+  // about 2^-16 relative, far below the bf16 rounding T and T' get next.
+  // X goes to Xs (fp32, row stride XS_LD).
   {
     if (tid < CH) {  // diagonal block R, column c: right-looking substitution
       const int R = tid >> 4, c = tid & 15, r0 = 16 * R;
@@ -755,26 +760,31 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     }
     __syncthreads();
     const int g = lane >> 2, t = lane & 3;
+    auto Af = [&](int r, int j) { return *reinterpret_cast<const float *>(KQ + af_off(r, j)); };
+    // fragments of a 16 x 16 A tile (rows r0.., columns k0..) and of a 16 x 8
+    // B tile of Xs (rows k0.., columns c0..), split into bf16 high and low parts
+    auto a_frags = [&](auto ld, int r0, int k0, uint32_t (&ah)[4], uint32_t (&al)[4]) {
+      split_bf16x2(ld(r0 + g, k0 + 2 * t), ld(r0 + g, k0 + 2 * t + 1), ah[0], al[0]);
+      split_bf16x2(ld(r0 + g + 8, k0 + 2 * t), ld(r0 + g + 8, k0 + 2 * t + 1), ah[1], al[1]);
+      split_bf16x2(ld(r0 + g, k0 + 2 * t + 8), ld(r0 + g, k0 + 2 * t + 9), ah[2], al[2]);
+      split_bf16x2(ld(r0 + g + 8, k0 + 2 * t + 8), ld(r0 + g + 8, k0 + 2 * t + 9), ah[3], al[3]);
+    };
+    auto Xf = [&](int r, int j) { return Xs[r * XS_LD + j]; };
+    auto b_frags = [&](int k0, int c0, uint32_t (&bh)[2], uint32_t (&bl)[2]) {
+      split_bf16x2(Xf(k0 + 2 * t, c0 + g), Xf(k0 + 2 * t + 1, c0 + g), bh[0], bl[0]);
+      split_bf16x2(Xf(k0 + 2 * t + 8, c0 + g), Xf(k0 + 2 * t + 9, c0 + g), bh[1], bl[1]);
+    };
     for (int R = 1; R < 4; ++R) {
       if (warp < 2 * R) {  // output X[R][K], columns 8 nh .. 8 nh + 7 of block K
         const int K = warp >> 1, c0 = 16 * K + 8 * (warp & 1), r0 = 16 * R;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int M = K; M < R; ++M) {
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const int ka = 16 * M + 8 * ks;
-            uint32_t ah[4], al[4], bh[2], bl[2];
-            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g, ka + t)), ah[0], al[0]);
-            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g + 8, ka + t)), ah[1], al[1]);
-            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g, ka + t + 4)), ah[2], al[2]);
-            split_tf32(*reinterpret_cast<const float *>(KQ + af_off(r0 + g + 8, ka + t + 4)), ah[3],
-                       al[3]);
-            split_tf32(Xs[(ka + t) * XS_LD + c0 + g], bh[0], bl[0]);
-            split_tf32(Xs[(ka + t + 4) * XS_LD + c0 + g], bh[1], bl[1]);
-            mma_tf32(acc, al, bh);
-            mma_tf32(acc, ah, bl);
-            mma_tf32(acc, ah, bh);
-          }
+          uint32_t ah[4], al[4], bh[2], bl[2];
+          a_frags(Af, r0, 16 * M, ah, al);
+          b_frags(16 * M, c0, bh, bl);
+          mma_bf16_16816(acc, al, bh);
+          mma_bf16_16816(acc, ah, bl);
+          mma_bf16_16816(acc, ah, bh);
         }
         // the sum over M goes where X[R][K] will be (this warp alone reads
         // and writes these 16 x 8 values), then X[R][K] = -X[R][R] (sum)
@@ -784,19 +794,13 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
         Xs[(r0 + g + 8) * XS_LD + c0 + 2 * t + 1] = acc[3];
         __syncwarp();
         float o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const int ka = r0 + 8 * ks;
+        {
           uint32_t ah[4], al[4], bh[2], bl[2];
-          split_tf32(Xs[(r0 + g) * XS_LD + ka + t], ah[0], al[0]);
-          split_tf32(Xs[(r0 + g + 8) * XS_LD + ka + t], ah[1], al[1]);
-          split_tf32(Xs[(r0 + g) * XS_LD + ka + t + 4], ah[2], al[2]);
-          split_tf32(Xs[(r0 + g + 8) * XS_LD + ka + t + 4], ah[3], al[3]);
-          split_tf32(Xs[(ka + t) * XS_LD + c0 + g], bh[0], bl[0]);
-          split_tf32(Xs[(ka + t + 4) * XS_LD + c0 + g], bh[1], bl[1]);
-          mma_tf32(o, al, bh);
-          mma_tf32(o, ah, bl);
-          mma_tf32(o, ah, bh);
+          a_frags(Xf, r0, r0, ah, al);
+          b_frags(r0, c0, bh, bl);
+          mma_bf16_16816(o, al, bh);
+          mma_bf16_16816(o, ah, bl);
+          mma_bf16_16816(o, ah, bh);
         }
         __syncwarp();  // every lane has read the sum before it is overwritten
         Xs[(r0 + g) * XS_LD + c0 + 2 * t] = -o[0];
