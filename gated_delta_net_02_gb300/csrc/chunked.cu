@@ -148,6 +148,10 @@ __device__ __forceinline__ uint32_t chunk16(int row, int cj) {
   return (uint32_t)(row * 128 + ((cj ^ (row & 7)) << 4));
 }
 
+__device__ __forceinline__ uint2 pack4(const float *x) {
+  return make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
+}
+
 __device__ __forceinline__ uint4 pack8(const float *x) {
   uint4 u;
   u.x = pack_bf16(x[0], x[1]);
@@ -301,6 +305,8 @@ constexpr int PREP_FAC = PREP_LAST + 256;           // GDA [64] row, [64] column
 constexpr int PREP_BAR = PREP_FAC + 512 + 32;       // 3 mbarriers
 constexpr int PREP_TSLOT = PREP_BAR + 24;
 constexpr int PREP_SMEM = PREP_TSLOT + 8 + 1024;    // + alignment slack
+constexpr int PREP_KTOT = (PREP_TSLOT + 8 + 15) & ~15;  // KDA [8 warps][128] f32 gate sums
+constexpr int PREP_SMEM_KDA = PREP_KTOT + 4096 + 1024;
 constexpr uint32_t PCOL_G = 0, PCOL_W = 0;          // TMEM columns (128 allocated; W reuses G's)
 static_assert(PREP_TZ % 1024 == 0 && PREP_KB % 1024 == 0, "swizzled atoms are 1024-aligned");
 static_assert(64 * XS_LD * 4 >= 16384, "X region also holds KB");
@@ -354,6 +360,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   float *srowf = reinterpret_cast<float *>(sm + PREP_FAC), *scolf = srowf + 64;
   float *srange = scolf + 64;
   int *sfact = reinterpret_cast<int *>(srange + 4);
+  float4 *ktot = reinterpret_cast<float4 *>(sm + PREP_KTOT);  // KDA only
   uint64_t *bar_tma = reinterpret_cast<uint64_t *>(sm + PREP_BAR);
   uint64_t *bar_g = bar_tma + 1, *bar_w = bar_tma + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + PREP_TSLOT);
@@ -407,24 +414,17 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
   const long long tile = tl;
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
-  // KDA gates, loaded while the tiles are in flight: thread = 8 channels
-  // (column chunk kc) x 4 consecutive rows (row group krg); the 16 row groups
-  // of a chunk are the 16 lanes of a half warp
-  const int kc = 2 * warp + (lane >> 4), krg = lane & 15;
-  float gk[KDA ? 4 : 1][8];
+  // KDA gates: warp = 8 consecutive rows, lane = 4 consecutive channels, so
+  // that every load (and every store of Q^ and K~ below) is one whole row
+  float gk[KDA ? 8 : 1][4];
   if constexpr (KDA) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = 4 * krg + k;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (r < len) {
-        const float4 *src =
-            reinterpret_cast<const float4 *>(g + ((long long)(t0 + r) * H + h) * DK + 8 * kc);
-        a = src[0];
-        b = src[1];
-      }
+    for (int k = 0; k < 8; ++k) {
+      const int r = 8 * warp + k;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < len)
+        a = *reinterpret_cast<const float4 *>(g + ((long long)(t0 + r) * H + h) * DK + 4 * lane);
       gk[k][0] = a.x; gk[k][1] = a.y; gk[k][2] = a.z; gk[k][3] = a.w;
-      gk[k][4] = b.x; gk[k][5] = b.y; gk[k][6] = b.z; gk[k][7] = b.w;
     }
   }
   if (tid < CH) {
@@ -482,6 +482,15 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     }
   }
   if (abort_flag) break;
+  if constexpr (KDA) {
+    // cumulative gates: prefix over the warp's 8 rows here, the sums of the
+    // warps before it after the barrier below
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) gk[k][c] += gk[k - 1][c];
+    ktot[warp * 32 + lane] = make_float4(gk[7][0], gk[7][1], gk[7][2], gk[7][3]);
+  }
   if (len < CH) {  // padding rows of K and Q are zero
     const int nz = (CH - len) * 8;
     for (int e = tid; e < nz * 2; e += PREP_THREADS) {
@@ -496,46 +505,40 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   if constexpr (KDA) {
     // Per-row decays inside the operands, relative to the chunk start:
     // K^ = e^g K and Q^ = e^g Q (A of G; K^ is also B of W), e^-g K (B of G),
-    // and for the scan Q^, K~ = e^(gC - g) K and e^gC. Cumulative gates:
-    // prefix over the thread's 4 rows, then over the 16 row groups of the
-    // chunk by shuffles within the half warp.
+    // and for the scan Q^, K~ = e^(gC - g) K and e^gC. The sums of the warps
+    // before this one complete the cumulative gates; all eight give gC.
+    float ex[4] = {0.f, 0.f, 0.f, 0.f}, gC[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 1; k < 4; ++k)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) gk[k][c] += gk[k - 1][c];
-    float gC[8], ex[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float x = gk[3][c];
-#pragma unroll
-      for (int d = 1; d < 16; d <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, d, 16);
-        if (krg >= d) x += y;
+    for (int w2 = 0; w2 < 8; ++w2) {
+      const float4 t = ktot[w2 * 32 + lane];
+      if (w2 < warp) {
+        ex[0] += t.x; ex[1] += t.y; ex[2] += t.z; ex[3] += t.w;
       }
-      ex[c] = x - gk[3][c];                               // rows before this group
-      gC[c] = __shfl_sync(0xffffffffu, x, 15, 16);        // whole chunk
+      gC[0] += t.x; gC[1] += t.y; gC[2] += t.z; gC[3] += t.w;
     }
     // out of range (NaN included): |gamma| > 80 at the chunk end or any row
     bool bad = false;
-    float eC[8];
+    float eC[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       bad |= !(fabsf(gC[c]) <= kMaxChunkLogDecay);
       eC[c] = __expf(gC[c]);
     }
-    const uint32_t half_off = (uint32_t)(kc >> 3) * 16384u, kb_off = (uint32_t)(kc >> 3) * 8192u;
+    // channels 4 lane .. 4 lane + 3: 64-column half, 16-byte piece, 8-byte half
+    const uint32_t half = (uint32_t)(lane >> 4), piece = (uint32_t)((lane & 15) >> 1);
+    const uint32_t sub = (uint32_t)(lane & 1) << 3;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = 4 * krg + k;
-      const uint32_t sw = (uint32_t)((((kc & 7) ^ (r & 7)) << 4) + r * 128);
-      uint4 *pk = reinterpret_cast<uint4 *>(KQ + half_off + sw);
-      uint4 *pq = reinterpret_cast<uint4 *>(KQ + half_off + 8192 + sw);
-      const uint4 ku = *pk, qu = *pq;
+    for (int k = 0; k < 8; ++k) {
+      const int r = 8 * warp + k;
+      const uint32_t sw = (uint32_t)r * 128u + ((piece ^ (uint32_t)(r & 7)) << 4) + sub;
+      uint2 *pk = reinterpret_cast<uint2 *>(KQ + half * 16384u + sw);
+      uint2 *pq = reinterpret_cast<uint2 *>(KQ + half * 16384u + 8192u + sw);
+      const uint2 ku = *pk, qu = *pq;
       const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ku);
       const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qu);
-      float kh[8], qh[8], kb[8], kt[8];
+      float kh[4], qh[4], kb[4], kt[4];
 #pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         const float2 kf = __bfloat1622float2(k2[c2]), qf = __bfloat1622float2(q2[c2]);
         const float kv[2] = {kf.x, kf.y}, qv[2] = {qf.x, qf.y};
 #pragma unroll
@@ -552,19 +555,17 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
           kt[c] = kv[e] * (eC[c] * e2);
         }
       }
-      const uint4 qhu = pack8(qh);
-      *pk = pack8(kh);
+      const uint2 qhu = pack4(qh);
+      *pk = pack4(kh);
       *pq = qhu;
-      *reinterpret_cast<uint4 *>(KB + kb_off + sw) = pack8(kb);
-      *reinterpret_cast<uint4 *>(w.Qh + (tile * CH + r) * DK + 8 * kc) = qhu;
-      *reinterpret_cast<uint4 *>(w.Kt + (tile * CH + r) * DK + 8 * kc) = pack8(kt);
+      *reinterpret_cast<uint2 *>(KB + half * 8192u + sw) = pack4(kb);
+      *reinterpret_cast<uint2 *>(w.Qh + (tile * CH + r) * DK + 4 * lane) = qhu;
+      *reinterpret_cast<uint2 *>(w.Kt + (tile * CH + r) * DK + 4 * lane) = pack4(kt);
     }
-    if (krg == 0) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        w.gs[tile * 256 + 128 + 8 * kc + c] = expf(gC[c]);
-        w.gs[tile * 256 + 8 * kc + c] = 1.f;
-      }
+    if (warp == 0) {
+      reinterpret_cast<float4 *>(w.gs + tile * 256 + 128)[lane] =
+          make_float4(expf(gC[0]), expf(gC[1]), expf(gC[2]), expf(gC[3]));
+      reinterpret_cast<float4 *>(w.gs + tile * 256)[lane] = make_float4(1.f, 1.f, 1.f, 1.f);
     }
     if (bad) set_error(err, kDevGateRange);
   } else {  // gate factors of the scan
@@ -1526,7 +1527,7 @@ cudaError_t set_attributes(int *num_sms) {
   const void *fns[] = {(const void *)chunk_prep_kernel<false>,
                        (const void *)chunk_prep_kernel<true>};
   for (const void *f : fns) {
-    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM_KDA);
     if (e != cudaSuccess) return e;
     // the whole unified L1 as shared memory, so that four CTAs fit per SM
     e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1619,7 +1620,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
       const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H,
                                                   (long long)num_sms * per_sm));
       if (a.kda)
-        chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
+        chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM_KDA, stream>>>(
             mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
       else
         chunk_prep_kernel<false><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
