@@ -148,6 +148,29 @@ __device__ __forceinline__ uint32_t chunk16(int row, int cj) {
   return (uint32_t)(row * 128 + ((cj ^ (row & 7)) << 4));
 }
 
+// In-place 4 x 4 transpose of 16-byte pieces inside each group of 4 lanes:
+// lane 4a + b holding pieces 0..3 of row 4a + b ends up with p[u] = piece b
+// of row 4a + u, so that store u of the group writes 64 contiguous bytes of
+// one row. Two xor-shuffle steps.
+__device__ __forceinline__ void transpose4x4(uint4 (&p)[4], int lane) {
+#pragma unroll
+  for (int m = 2; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if (b & m) continue;
+      const uint4 snd = hi ? p[b] : p[b | m];
+      uint4 rcv;
+      rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+      rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+      rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+      rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+      if (hi) p[b] = rcv;
+      else p[b | m] = rcv;
+    }
+  }
+}
+
 __device__ __forceinline__ uint2 pack4(const float *x) {
   return make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
 }
@@ -707,11 +730,15 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
           packed[u / 2] = pack_bf16(p0, p1);
         }
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(w.P + (tile * CH + r) * CH + j0);
+      uint4 pc[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2],
-                            packed[4 * e + 3]);
+        pc[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+      transpose4x4(pc, lane);  // each store: 64 contiguous bytes of 8 rows
+      const int rb = r - (lane & 3);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        reinterpret_cast<uint4 *>(w.P + (tile * CH + rb + u) * CH + j0)[lane & 3] = pc[u];
     }
   }
   tc_fence_before();
@@ -813,27 +840,32 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     }
   }
   // T[r][j] = X[r][j] beta_j (to the workspace) and T'[r][j] = X[r][j] f_j
-  // into TZ; thread = (row r, 16 columns)
+  // into TZ; thread = (row r = tid / 4, columns 8q..8q+7 and 8q+32..8q+39 with
+  // q = tid % 4), so that each store of a warp writes 64 contiguous bytes of
+  // each of 8 rows
   {
-    const int r = tid & 63, qd = tid >> 6;
+    const int r = tid >> 2, q = tid & 3;
     float tv[16], tp[16];
-    const float4 *xr = reinterpret_cast<const float4 *>(Xs + r * XS_LD + 16 * qd);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const float4 x4 = xr[v];
-      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const float4 *xr = reinterpret_cast<const float4 *>(Xs + r * XS_LD + 8 * q + 32 * hlf);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int j = 16 * qd + 4 * v + b;
-        tv[4 * v + b] = xv[b] * sbeta[j];
-        tp[4 * v + b] = xv[b] * stf[j];
+      for (int v = 0; v < 2; ++v) {
+        const float4 x4 = xr[v];
+        const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int j = 8 * q + 32 * hlf + 4 * v + b;
+          tv[8 * hlf + 4 * v + b] = xv[b] * sbeta[j];
+          tp[8 * hlf + 4 * v + b] = xv[b] * stf[j];
+        }
       }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(w.T + (tile * CH + r) * CH + 16 * qd);
-    dst[0] = pack8(tv);
-    dst[1] = pack8(tv + 8);
-    *reinterpret_cast<uint4 *>(TZ + chunk16(r, 2 * qd)) = pack8(tp);
-    *reinterpret_cast<uint4 *>(TZ + chunk16(r, 2 * qd + 1)) = pack8(tp + 8);
+    uint4 *dst = reinterpret_cast<uint4 *>(w.T + (tile * CH + r) * CH);
+    dst[q] = pack8(tv);
+    dst[q + 4] = pack8(tv + 8);
+    *reinterpret_cast<uint4 *>(TZ + chunk16(r, q)) = pack8(tp);
+    *reinterpret_cast<uint4 *>(TZ + chunk16(r, q + 4)) = pack8(tp + 8);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -862,15 +894,21 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   tc_fence_after();
   if (!abort_flag && (warp & 3) < 2) {  // -W: rows r (lanes 0..63), 64 columns per warp
     const int r = 32 * (warp & 3) + lane, c0 = 64 * (warp >> 2);
-    uint4 *dst = reinterpret_cast<uint4 *>(w.W + (tile * CH + r) * DK + c0);
+    const int rb = r - (lane & 3);
 #pragma unroll
     for (int q32 = 0; q32 < 2; ++q32) {
       float v[32];
       tmem_ld32(tbase + ((uint32_t)(32 * (warp & 3)) << 16) + PCOL_W + c0 + 32 * q32, v);
 #pragma unroll
       for (int u = 0; u < 32; ++u) v[u] = -v[u];
+      uint4 pc[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dst[4 * q32 + q] = pack8(v + 8 * q);
+      for (int q = 0; q < 4; ++q) pc[q] = pack8(v + 8 * q);
+      transpose4x4(pc, lane);  // each store: 64 contiguous bytes of 8 rows
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        reinterpret_cast<uint4 *>(w.W + (tile * CH + rb + u) * DK + c0 + 32 * q32)[lane & 3] =
+            pc[u];
     }
   }
   tc_fence_before();
