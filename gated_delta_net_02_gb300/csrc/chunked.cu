@@ -419,22 +419,26 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   // Persistent: every CTA takes the next unclaimed tile (tiles go in chunk
   // order) from the counter in hdr[1]; the copies of its next tile are issued
   // as soon as the current one's last product has read K and Q. Thread 0
-  // claims, and counts the loads issued and waited for.
-  __shared__ int next_tile, s_claim[2];
+  // claims, and counts the loads issued and waited for; the first token and
+  // length of the next tile's chunk are read with the claim and handed over
+  // in shared memory.
+  __shared__ int next_tile, next_tok, next_len, s_claim[3];
   int loads_issued = 0, loads_done = 0;
   if (tid == 0) {
     const int t = atomicAdd(&w.hdr[1], 1);
     next_tile = t;
     if (t < ntiles) {
-      load_tile(t, w.chunk_tok[t / H]);
+      next_tok = w.chunk_tok[t / H];
+      next_len = w.chunk_len[t / H];
+      load_tile(t, next_tok);
       loads_issued = 1;
     }
   }
   __syncthreads();
   for (int it = 0, tl = next_tile; tl < ntiles; ++it) {
   const uint32_t par = (uint32_t)(it & 1);
-  const int c = tl / H, h = tl % H;
-  const int t0 = w.chunk_tok[c], len = w.chunk_len[c];
+  const int h = tl % H;
+  const int t0 = next_tok, len = next_len;
   const long long tile = tl;
   // gates and beta while the tiles are in flight (padding rows: g = beta = 0)
   // KDA gates: warp = 8 consecutive rows, lane = 4 consecutive channels, so
@@ -652,7 +656,10 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       umma_bf16(tbase + PCOL_G, sdesc_kmajor(a0 + (s >> 2) * 16384u + (s & 3) * 32u),
                 sdesc_kmajor(b0 + (s >> 2) * bcol + (s & 3) * 32u), idesc, s > 0);
     umma_commit(bar_g);
-    if (s_claim[0] < ntiles) s_claim[1] = w.chunk_tok[s_claim[0] / H];
+    if (s_claim[0] < ntiles) {
+      s_claim[1] = w.chunk_tok[s_claim[0] / H];
+      s_claim[2] = w.chunk_len[s_claim[0] / H];
+    }
     if (!mbar_wait(bar_g, par, err, kSitePrepG)) abort_flag = 1;
   }
   __syncthreads();
@@ -885,6 +892,8 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     } else {  // K and Q are free: the next tile's copies
       next_tile = s_claim[0];
       if (s_claim[0] < ntiles) {
+        next_tok = s_claim[1];
+        next_len = s_claim[2];
         load_tile(s_claim[0], s_claim[1]);
         ++loads_issued;
       }
@@ -1105,6 +1114,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   const int nch = w.seq_nch[s];
   if (nch == 0) return;
   const int chunk0 = w.seq_chunk0[s];
+  // chunk j of the sequence starts at token tok0 + 64 j, and only the last
+  // one can be partial (work-list layout): no per-chunk metadata loads
+  const int tok0 = w.chunk_tok[chunk0], last_len = w.chunk_len[chunk0 + nch - 1];
+  auto chunk_len_of = [&](int j) { return j == nch - 1 ? last_len : CH; };
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
@@ -1164,7 +1177,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       }
       unsigned char *base = sm + st * ST_BYTES;
       const int gc = chunk0 + jc;
-      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      const int t0 = tok0 + CH * jc, len = chunk_len_of(jc);
       const int trow = (gc * H + h) * CH;
       if (wait_ready) {  // the tiles of chunk gc, head h are written
         int ok = 1;
@@ -1192,7 +1205,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         tma_load_2d(base + ST_P, &map_P, 0, trow, fb);
         bulk_g2s(base + ST_G, w.gs + ((long long)gc * H + h) * 256, 1024, fb);
         if (jc + 2 < nch) {  // chunk jc + 2 loads into this stage two chunks later: warm L2
-          const int gp = gc + 2, tp = w.chunk_tok[gp], prow = (gp * H + h) * CH;
+          const int gp = gc + 2, tp = tok0 + CH * (jc + 2), prow = (gp * H + h) * CH;
           if constexpr (KDA) {
             tma_prefetch_2d(&map_k, 0, prow);
             tma_prefetch_2d(&map_k, 64, prow);
@@ -1248,7 +1261,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, true, true);
       // stage of chunk j usable: landed, or for a partial last chunk padded
       auto stage_bar = [&](int j, uint32_t *parity) -> uint64_t * {
-        if (w.chunk_len[chunk0 + j] < CH) {
+        if (chunk_len_of(j) < CH) {
           *parity = 0;
           return bE1;
         }
@@ -1360,8 +1373,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     // before the barrier that precedes the next writes); a partial last
     // chunk is stored row by row, so no token past its end is touched.
     auto store_out = [&](int j, float qf) {
-      const int gc = chunk0 + j;
-      const int t0 = w.chunk_tok[gc], len = w.chunk_len[gc];
+      const int t0 = tok0 + CH * j, len = chunk_len_of(j);
       if ((warp & 3) >= 2) {
         const int r = i - CH;
         float xv[32], ov[32];
@@ -1449,7 +1461,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       if (tid == 0 && jc + 1 < nch) mbar_arrive(bE4);
       // checkpoint: the state after a full chunk that ends on a multiple of
       // ckpt_every tokens (chunks start at multiples of 64 in the sequence)
-      if (CKPT && w.chunk_len[chunk0 + jc] == CH) {
+      if (CKPT && chunk_len_of(jc) == CH) {
         const int pos = (jc + 1) * CH, c = pos / ckpt_every - 1;
         if (pos % ckpt_every == 0 && c < max_ckpts)
           store_rows32(Sm,
