@@ -492,14 +492,15 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
       smin[tid] = mn;
     }
   }
-  // thread 0: the tile after this one and its first token, claimed and read
-  // early so that the atomic's and the load's latencies hide behind this tile
-  // (kept in shared memory: no registers live across the tile)
+  // thread 0 waits for this tile's copies; thread 64 (idle until the barrier
+  // below) claims the tile after this one, so that the two latencies overlap
+  // and the claim is known long before its copies are issued (kept in shared
+  // memory: no registers live across the tile)
   if (tid == 0) {
     if (mbar_wait(bar_tma, par, err, kSitePrepLoad)) ++loads_done;
     else abort_flag = 1;
-    s_claim[0] = one_tile ? ntiles : atomicAdd(&w.hdr[1], 1);
   }
+  if (tid == 64) s_claim[0] = one_tile ? ntiles : atomicAdd(&w.hdr[1], 1);
   __syncthreads();
   if constexpr (!KDA) {
     if (tid >= 32 && tid < CH) {
