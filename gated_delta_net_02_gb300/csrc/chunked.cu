@@ -211,6 +211,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 // ---- 1. work list ---------------------------------------------------------------
 
 constexpr int WL_THREADS = 1024;
+constexpr int WL_SMEM_SEQS = 4096;  // cu_seqlens read into shared memory up to this many sequences
 
 // One block. Validates cu_seqlens (cu[0] = 0, non-decreasing, cu[N] = Ntok);
 // hdr[0] = chunks in use, hdr[1] = chunk prep's tile counter (zeroed here);
@@ -222,17 +223,28 @@ __global__ void __launch_bounds__(WL_THREADS)
     worklist_kernel(const int32_t *__restrict__ cu, int N, int total, int K, int H,
                     long long state_elems, const float *const *state_in, WsPtrs w,
                     long long n_ready, int *err) {
+  // The kernels after this one are programmatic dependents: they may start
+  // their set-up now and wait for this grid before reading what it writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int bad;
-  __shared__ int part[WL_THREADS];
-  const int tid = threadIdx.x;
+  __shared__ int wsum[WL_THREADS / 32];
+  __shared__ int scu[WL_SMEM_SEQS + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool in_smem = N <= WL_SMEM_SEQS;
+  auto CU = [&](int i) { return in_smem ? scu[i] : cu[i]; };
   // chunk prep's tile counter, and the per-tile ready flags when the scan
   // runs beside the prep
-  if (tid == 0) w.hdr[1] = 0;
+  if (tid == 0) {
+    w.hdr[1] = 0;
+    bad = 0;
+  }
   for (long long e = tid; e < n_ready; e += WL_THREADS) w.ready[e] = 0;
-  if (tid == 0) bad = (cu[0] != 0 || cu[N] != total) ? 1 : 0;
+  if (in_smem)
+    for (int i = tid; i <= N; i += WL_THREADS) scu[i] = cu[i];
   __syncthreads();
+  if (tid == 0 && (CU(0) != 0 || CU(N) != total)) bad = 1;
   for (int s = tid; s < N; s += WL_THREADS)
-    if (cu[s + 1] < cu[s]) bad = 1;
+    if (CU(s + 1) < CU(s)) bad = 1;
   __syncthreads();
   if (bad) {
     if (tid == 0) {
@@ -251,52 +263,64 @@ __global__ void __launch_bounds__(WL_THREADS)
     return;
   }
   // per-thread contiguous segment of sequences, then a block scan of counts
+  // (inclusive scans within each warp, then over the warps' totals)
   const int per = (N + WL_THREADS - 1) / WL_THREADS;
   const int s0 = min(N, tid * per), s1 = min(N, s0 + per);
   int cnt = 0;
   for (int s = s0; s < s1; ++s) {
-    const int L = cu[s + 1] - cu[s];
+    const int L = CU(s + 1) - CU(s);
     const int Lc = max(L - K, 0);
     cnt += (Lc + CH - 1) / CH;
   }
-  part[tid] = cnt;
-  __syncthreads();
-  for (int off = 1; off < WL_THREADS; off <<= 1) {  // Hillis-Steele inclusive scan
-    const int v = tid >= off ? part[tid - off] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
   }
-  int base = part[tid] - cnt;
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += y;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  if (warp > 0) incl += wsum[warp - 1];
+  int base = incl - cnt;
   for (int s = s0; s < s1; ++s) {
-    const int L = cu[s + 1] - cu[s];
+    const int L = CU(s + 1) - CU(s);
     const int Lc = max(L - K, 0);
     const int nch = (Lc + CH - 1) / CH;
     w.seq_chunk0[s] = base;
     w.seq_nch[s] = nch;
-    w.tail_start[s] = cu[s] + Lc;
+    w.tail_start[s] = CU(s) + Lc;
     w.tail_len[s] = L - Lc;
     w.tail_pos[s] = Lc;  // position of the first tail token within the sequence
     w.state_ptrs[s] = nch > 0 ? w.states + (long long)s * state_elems : state_in[s];
     for (int j = 0; j < nch; ++j) {
       w.chunk_seq[base + j] = s;
-      w.chunk_tok[base + j] = cu[s] + j * CH;
+      w.chunk_tok[base + j] = CU(s) + j * CH;
       w.chunk_len[base + j] = min(CH, Lc - j * CH);
     }
     base += nch;
   }
-  if (tid == WL_THREADS - 1) w.hdr[0] = part[WL_THREADS - 1];
+  if (tid == WL_THREADS - 1) w.hdr[0] = incl;
   // longest chunk count first (ties by index); identity beyond 4096 sequences
   for (int s = tid; s < N; s += WL_THREADS) {
     if (N > 4096) {
       w.order[s] = s;
       continue;
     }
-    const int L = cu[s + 1] - cu[s];
+    const int L = CU(s + 1) - CU(s);
     const int ns = (max(L - K, 0) + CH - 1) / CH;
     int rank = 0;
     for (int t = 0; t < N; ++t) {
-      const int Lt = cu[t + 1] - cu[t];
+      const int Lt = CU(t + 1) - CU(t);
       const int nt = (max(Lt - K, 0) + CH - 1) / CH;
       rank += (nt > ns) || (nt == ns && t < s);
     }
@@ -355,8 +379,11 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
                       const float *__restrict__ beta, int H, int Hqk, int qk_grouped,
                       WsPtrs w, int publish, int handoff_sms, int num_sms, int *err) {
   constexpr int DK = 128;
-  // A chunk scan launched after this grid as a programmatic dependent may
-  // start once every CTA here has started (hand-off mode, see below).
+  // This grid is a programmatic dependent of the work list: wait for it
+  // before reading what it wrote. The chunk scan, launched after this grid as
+  // a programmatic dependent, may then start once every CTA here has passed
+  // this point (so the work list is complete for it too).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ntiles = w.hdr[0] * H;  // (chunks in use) x heads, chunk-major
   if ((int)blockIdx.x >= ntiles) return;
@@ -1104,10 +1131,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       int Hqk, int qk_grouped, float scale, WsPtrs w, float *ckpt,
                       int ckpt_every, int max_ckpts, int wait_ready, int *err) {
   constexpr int DK = 128, DV = 128;
-  // With wait_ready this grid is a programmatic dependent of the chunk prep,
-  // which is still running: the work list (an earlier kernel) is complete,
-  // and each chunk's tiles are read only after their ready flags (no
-  // griddepcontrol.wait, which would wait for the whole prep).
+  // This grid is a programmatic dependent of the chunk prep. With wait_ready
+  // the prep is still running beside it: the work list is complete (every
+  // prep CTA waited for it before this grid could start), and each chunk's
+  // tiles are read only after their ready flags. Otherwise it waits for the
+  // whole prep here. The recurrent tail after it may start its own set-up
+  // now; it waits for this grid before reading the states.
+  if (!wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
   const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
@@ -1667,54 +1698,38 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     // persistent prep CTAs: as many as fit at once (registers allow three per
     // SM for per-row gates, four for scalar gates; four use all of TMEM)
     const int per_sm = a.kda ? 3 : 4;
+    // Work list -> prep -> scan -> tail are programmatic dependent launches:
+    // each kernel's launch and set-up overlap the previous one's drain, and
+    // each waits (griddepcontrol.wait) before reading what that one wrote.
     auto launch_prep = [&](int publish, int handoff) -> cudaError_t {
       const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H,
                                                   (long long)num_sms * per_sm));
       if (a.kda)
-        chunk_prep_kernel<true><<<g3, PREP_THREADS, PREP_SMEM_KDA, stream>>>(
-            mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
-      else
-        chunk_prep_kernel<false><<<g3, PREP_THREADS, PREP_SMEM, stream>>>(
-            mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
-      return cudaGetLastError();
+        return launch_pdl(chunk_prep_kernel<true>, g3, dim3(PREP_THREADS), PREP_SMEM_KDA,
+                          stream, mq, mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff,
+                          num_sms, a.err);
+      return launch_pdl(chunk_prep_kernel<false>, g3, dim3(PREP_THREADS), PREP_SMEM, stream, mq,
+                        mk, a.g, a.beta, a.H, Hqk, qg, w, publish, handoff, num_sms, a.err);
     };
     const long long scan_grid = (long long)a.n_seqs * a.H * 2;
     auto launch_scan = [&](int wait_ready) -> cudaError_t {
       const dim3 sg((unsigned)scan_grid), st(SCAN_THREADS);
       const int ce = a.ckpt ? a.ckpt_every : 1, cm = a.ckpt ? a.max_ckpts : 0;
-      // as a programmatic dependent of the prep when it waits for ready flags
       if (a.kda && a.ckpt)
-        return wait_ready ? launch_pdl(chunk_scan_kernel<true, true>, sg, st, SCAN_SMEM, stream,
-                                       mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
-                                       qg, a.scale, w, a.ckpt, ce, cm, wait_ready, a.err)
-                          : (chunk_scan_kernel<true, true><<<sg, st, SCAN_SMEM, stream>>>(
-                                 mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
-                                 a.scale, w, a.ckpt, ce, cm, wait_ready, a.err),
-                             cudaGetLastError());
+        return launch_pdl(chunk_scan_kernel<true, true>, sg, st, SCAN_SMEM, stream, mKt, mQh, mv,
+                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+                          ce, cm, wait_ready, a.err);
       if (a.kda)
-        return wait_ready ? launch_pdl(chunk_scan_kernel<true, false>, sg, st, SCAN_SMEM, stream,
-                                       mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
-                                       qg, a.scale, w, (float *)nullptr, ce, cm, wait_ready,
-                                       a.err)
-                          : (chunk_scan_kernel<true, false><<<sg, st, SCAN_SMEM, stream>>>(
-                                 mKt, mQh, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
-                                 a.scale, w, nullptr, ce, cm, wait_ready, a.err),
-                             cudaGetLastError());
+        return launch_pdl(chunk_scan_kernel<true, false>, sg, st, SCAN_SMEM, stream, mKt, mQh,
+                          mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w,
+                          (float *)nullptr, ce, cm, wait_ready, a.err);
       if (a.ckpt)
-        return wait_ready ? launch_pdl(chunk_scan_kernel<false, true>, sg, st, SCAN_SMEM, stream,
-                                       mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk,
-                                       qg, a.scale, w, a.ckpt, ce, cm, wait_ready, a.err)
-                          : (chunk_scan_kernel<false, true><<<sg, st, SCAN_SMEM, stream>>>(
-                                 mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
-                                 a.scale, w, a.ckpt, ce, cm, wait_ready, a.err),
-                             cudaGetLastError());
-      return wait_ready ? launch_pdl(chunk_scan_kernel<false, false>, sg, st, SCAN_SMEM, stream,
-                                     mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
-                                     a.scale, w, (float *)nullptr, ce, cm, wait_ready, a.err)
-                        : (chunk_scan_kernel<false, false><<<sg, st, SCAN_SMEM, stream>>>(
-                               mk, mq, mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg,
-                               a.scale, w, nullptr, ce, cm, wait_ready, a.err),
-                           cudaGetLastError());
+        return launch_pdl(chunk_scan_kernel<false, true>, sg, st, SCAN_SMEM, stream, mk, mq, mv,
+                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+                          ce, cm, wait_ready, a.err);
+      return launch_pdl(chunk_scan_kernel<false, false>, sg, st, SCAN_SMEM, stream, mk, mq, mv,
+                        mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w,
+                        (float *)nullptr, ce, cm, wait_ready, a.err);
     };
     // The prep runs first, on every SM. When the scan (one CTA per SM)
     // leaves at least an eighth of the SMs free, it is launched right behind
