@@ -1510,7 +1510,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       tc_fence_before();
     }
     if (tid == 0) bulk_wait_all();
-    if (!*abort_flag) {  // state after the chunked part, read by the tail
+    if (!*abort_flag) {  // state after the chunked part: read by the tail, or the slot itself
       float4 *dst = reinterpret_cast<float4 *>(
           w.states + (((long long)s * H + h) * DK + i) * DV + NV * vs + 32 * ch);
 #pragma unroll
@@ -1674,10 +1674,16 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
   if (a.workspace_bytes < lay.total) return cudaErrorInvalidValue;
   const WsPtrs w = ws_ptrs(a.workspace, lay);
   const long long state_elems = (long long)a.H * a.Dk * a.Dv;
+  // With one slot, the slot is the final state: the chunked part takes every
+  // token, the scan writes its final state straight into the slot (same
+  // [N][H][D_k][D_v] layout as the workspace states), and no tail runs.
+  const bool direct = a.n_slots == 1;
+  WsPtrs ws = w;
+  if (direct) ws.states = a.slots;
 
   worklist_kernel<<<1, WL_THREADS, 0, stream>>>(a.cu_seqlens, a.n_seqs, a.total_tokens,
-                                                a.n_slots, a.H, state_elems, a.state_in, w,
-                                                lay.max_chunks * a.H, a.err);
+                                                direct ? 0 : a.n_slots, a.H, state_elems,
+                                                a.state_in, w, lay.max_chunks * a.H, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (a.total_tokens > 0) {
@@ -1717,18 +1723,18 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
       const int ce = a.ckpt ? a.ckpt_every : 1, cm = a.ckpt ? a.max_ckpts : 0;
       if (a.kda && a.ckpt)
         return launch_pdl(chunk_scan_kernel<true, true>, sg, st, SCAN_SMEM, stream, mKt, mQh, mv,
-                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, ws, a.ckpt,
                           ce, cm, wait_ready, a.err);
       if (a.kda)
         return launch_pdl(chunk_scan_kernel<true, false>, sg, st, SCAN_SMEM, stream, mKt, mQh,
-                          mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w,
+                          mv, mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, ws,
                           (float *)nullptr, ce, cm, wait_ready, a.err);
       if (a.ckpt)
         return launch_pdl(chunk_scan_kernel<false, true>, sg, st, SCAN_SMEM, stream, mk, mq, mv,
-                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w, a.ckpt,
+                          mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, ws, a.ckpt,
                           ce, cm, wait_ready, a.err);
       return launch_pdl(chunk_scan_kernel<false, false>, sg, st, SCAN_SMEM, stream, mk, mq, mv,
-                        mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, w,
+                        mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, ws,
                         (float *)nullptr, ce, cm, wait_ready, a.err);
     };
     // The prep runs first, on every SM. When the scan (one CTA per SM)
@@ -1746,6 +1752,7 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
+  if (direct) return cudaSuccess;
   // the last n_slots tokens of every sequence: token loop with snapshots
   RecurrentArgs r{};
   r.q = a.q; r.k = a.k; r.v = a.v; r.g = a.g; r.beta = a.beta;

@@ -134,8 +134,10 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
  *    sequence run through the chunked (chunk 64, WY/UT-transform)
  *    tensor-core kernels, with the last partial chunk padded by no-op rows;
  *    the last n_slots tokens run through the recurrent kernel, which writes
- *    the slots. The result equals the token recurrence up to rounding (bf16
- *    tensor-core operands, fp32 accumulation and fp32 state).
+ *    the slots. With n_slots = 1 the slot is the final state, so every token
+ *    runs through the chunked kernels, which write it. The result equals the
+ *    token recurrence up to rounding (bf16 tensor-core operands, fp32
+ *    accumulation and fp32 state).
  *  - fp32 inputs (whose 1e-5 accuracy bf16 operands cannot meet) and head
  *    sizes of 64: every token runs through the recurrent kernel on the GPU,
  *    as the pages' chunked path also falls back to the token loop ("Enable
