@@ -1144,7 +1144,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   const int hq = qk_grouped ? h / (H / Hqk) : h % Hqk;  // q/k head of value head h
   const int s = w.order[(blockIdx.x >> 1) / H];
   const int nch = w.seq_nch[s];
-  if (nch == 0) return;
+  if (nch == 0) {
+    if (wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");  // see the end
+    return;
+  }
   const int chunk0 = w.seq_chunk0[s];
   // chunk j of the sequence starts at token tok0 + 64 j, and only the last
   // one can be partial (work-list layout): no per-chunk metadata loads
@@ -1518,6 +1521,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
     }
   }
+  // Beside the prep, nothing else orders the prep's completion before this
+  // grid's: wait for it here (it has long finished), so that whatever runs
+  // after this grid in the stream finds the prep complete as well.
+  if (wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
