@@ -96,6 +96,31 @@ LENS = [700, 257, 64, 191, 9, 0, 320]
 
 
 @pytest.mark.parametrize("mode", ["gda", "kda"])
+def test_one_slot_checkpoints(gdn, mode):
+    """One slot: the chunk scan covers every token and writes the slot itself
+    (no token-loop tail), so a checkpoint on a sequence's last token comes from
+    the scan too. Lengths ending on a boundary (320, 256, 64), ragged (257,
+    191, 9) and empty."""
+    lens = [320, 257, 256, 191, 64, 9, 0]
+    every, max_ckpts = 64, 6
+    b = inputs.make_batch(77, lens, 2, 128, 128, mode=mode, n_slots=1)
+    out, slots, cks = run(gdn, b, every, max_ckpts)
+    assert check_checkpoints(b, cks, every, max_ckpts, TOL[torch.bfloat16]) > 0
+    final = oracle_prefix_state(b, b.seq_len.numpy())
+    L = b.seq_len.numpy()
+    have = L > 0
+    sl = slots.double().cpu().numpy()
+    assert rel_l2(sl[have, 0], final[have]) <= TOL[torch.bfloat16]
+    assert np.isnan(sl[~have]).all()
+    for s, n in enumerate(L):  # a checkpoint on the last token is the slot itself
+        if n > 0 and n % every == 0 and n // every <= max_ckpts:
+            assert torch.equal(cks[s, n // every - 1], slots[s, 0])
+    out0, slots0, _ = run(gdn, b, every, max_ckpts, ckpt=False)
+    assert torch.equal(out.nan_to_num(7.0), out0.nan_to_num(7.0))
+    assert torch.equal(slots.nan_to_num(7.0), slots0.nan_to_num(7.0))
+
+
+@pytest.mark.parametrize("mode", ["gda", "kda"])
 @pytest.mark.parametrize("every,max_ckpts", [(64, 12), (128, 2)])
 def test_checkpoints_match_oracle_bf16(gdn, mode, every, max_ckpts):
     b = inputs.make_batch(71, LENS, 2, 128, 128, mode=mode, n_slots=4)
