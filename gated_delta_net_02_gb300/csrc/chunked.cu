@@ -1668,6 +1668,7 @@ static cudaError_t launch_token_loop(const ChunkedArgs &a, cudaStream_t stream) 
   r.Hqk = a.Hqk > 0 ? a.Hqk : a.H; r.qk_grouped = a.qk_grouped;
   r.n_slots = a.n_slots; r.kda = a.kda; r.bf16 = a.bf16; r.scale = a.scale; r.err = a.err;
   r.ckpt = a.ckpt; r.pos0 = w.tail_pos; r.ckpt_every = a.ckpt_every; r.max_ckpts = a.max_ckpts;
+  r.long_chains = true;
   return launch_recurrent(r, stream);
 }
 

@@ -31,6 +31,10 @@ struct RecurrentArgs {
   // programmatic launch (gdn_forward only: tok_start and seq_len must be NULL,
   // since the kernel reads its scalars before waiting for its predecessor)
   bool pdl = false;
+  // long serial chains (the chunked call's token-loop route): 128 x 128
+  // heads with fp32 inputs take a narrower slice per CTA (16 lanes across
+  // the key rows, 32 columns), which shortens each token's step
+  bool long_chains = false;
 };
 
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);

@@ -43,6 +43,7 @@ struct RecParams {
   int Hqk, qk_grouped;  // q/k heads and the value-head -> q/k-head map
   float *ckpt;          // optional checkpoints, [n_seqs][max_ckpts][H][Dk][Dv]
   int pdl;              // launched programmatically (tok_start, seq_len, ckpt NULL)
+  int long_chains;      // see RecurrentArgs
   const int *pos0;      // position of each sequence's first token (NULL = 0)
   int ckpt_every, max_ckpts;
   float scale;
@@ -337,8 +338,10 @@ __global__ void __launch_bounds__(C::NT)
   }
 }
 
-// Kernel configuration per head size. Fixed per (D_k, D_v) so that the
-// arithmetic order never depends on T, K or the batch.
+// Kernel configuration per head size. Fixed per (D_k, D_v) and input type so
+// that the arithmetic order never depends on T, K or the batch (the chunked
+// call's fp32 token loop, 128 x 128 heads, takes its own fixed configuration:
+// see launch_d).
 template <int DK, int DV, bool KDA, typename Tin>
 struct RecPick;
 template <bool KDA, typename Tin>
@@ -350,9 +353,8 @@ struct RecPick<64, 128, KDA, Tin> { using C = RecCfg<64, 128, 4, 2, KDA, Tin>; }
 template <bool KDA, typename Tin>
 struct RecPick<64, 64, KDA, Tin> { using C = RecCfg<64, 64, 4, 2, KDA, Tin>; };
 
-template <int DK, int DV, bool KDA, typename Tin>
-cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
-  using C = typename RecPick<DK, DV, KDA, Tin>::C;
+template <typename C>
+cudaError_t launch_c(const RecParams &p, cudaStream_t stream) {
   const long long n_items = (long long)p.n_seqs * p.H * C::CTAS_PER_HEAD;
   if (n_items == 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -367,8 +369,20 @@ cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int DK, int DV, bool KDA, typename Tin>
+cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
+  return launch_c<typename RecPick<DK, DV, KDA, Tin>::C>(p, stream);
+}
+
 template <int DK, int DV>
 cudaError_t launch_d(const RecParams &p, bool kda, bool bf16, cudaStream_t s) {
+  if constexpr (DK == 128 && DV == 128) {
+    // long fp32 chains: a token's step is latency-bound, and a narrower slice
+    // per CTA shortens it (about 10% on the varlen fp32 prefill)
+    if (p.long_chains && !bf16)
+      return kda ? launch_c<RecCfg<128, 128, 16, 4, true, float>>(p, s)
+                 : launch_c<RecCfg<128, 128, 16, 4, false, float>>(p, s);
+  }
   if (kda)
     return bf16 ? launch_t<DK, DV, true, __nv_bfloat16>(p, s)
                 : launch_t<DK, DV, true, float>(p, s);
@@ -389,6 +403,7 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
   p.qk_grouped = a.qk_grouped ? 1 : 0;
   p.ckpt = a.ckpt; p.pos0 = a.pos0;
   p.pdl = a.pdl && !a.tok_start && !a.seq_len && !a.ckpt ? 1 : 0;
+  p.long_chains = a.long_chains ? 1 : 0;
   p.ckpt_every = a.ckpt_every > 0 ? a.ckpt_every : 1; p.max_ckpts = a.max_ckpts;
   p.scale = a.scale; p.err = a.err;
   if (a.Dk == 128 && a.Dv == 128) return launch_d<128, 128>(p, a.kda, a.bf16, stream);
