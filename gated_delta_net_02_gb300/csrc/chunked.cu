@@ -1745,15 +1745,18 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
                         mT, mP, mW, mo, a.state_in, a.out, a.H, Hqk, qg, a.scale, ws,
                         (float *)nullptr, ce, cm, wait_ready, a.err);
     };
-    // The prep runs first, on every SM. When the scan (one CTA per SM)
-    // leaves at least an eighth of the SMs free, it is launched right behind
-    // the prep as a programmatic dependent ("hand-off"): the prep CTAs on as
-    // many SMs as the scan has CTAs take one tile each and leave, the scan's
-    // CTAs take those SMs and wait for each tile's ready flag while the rest
-    // of the prep goes on. The scan can start only once every prep CTA has
-    // started, and the prep never waits on the scan, so the prep always
-    // finishes. Otherwise the scan simply runs after the prep.
-    const bool handoff = scan_grid <= num_sms - std::max(16, num_sms / 8);
+    // The prep runs first, on every SM. When the scan (one CTA per SM) needs
+    // at most half of the SMs, it is launched right behind the prep as a
+    // programmatic dependent ("hand-off"): the prep CTAs on as many SMs as the
+    // scan has CTAs take one tile each and leave, the scan's CTAs take those
+    // SMs and wait for each tile's ready flag while the rest of the prep goes
+    // on. The scan can start only once every prep CTA has started, and the
+    // prep never waits on the scan, so the prep always finishes. With more
+    // scan CTAs the prep left on the other SMs cannot keep up with the chains
+    // (a schedule model with the measured rates puts the break-even between
+    // 80 and 96 scan CTAs for either gate mode, and a 128-CTA scan 3x slower
+    // beside the prep than after it), so the scan simply runs after the prep.
+    const bool handoff = 2 * scan_grid <= num_sms;
     if ((e = launch_prep(handoff ? 1 : 0, handoff ? (int)scan_grid : 0)) != cudaSuccess)
       return e;
     if ((e = launch_scan(handoff ? 1 : 0)) != cudaSuccess) return e;
