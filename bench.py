@@ -13,7 +13,12 @@ line on rank 0. Inputs are resident in HBM when the timed region starts; the
 inputs of every workload are larger than the L2 (decode rotates over enough
 state banks that every step reads its state from HBM). The "e2e" figure
 repeats the measurement with each step's inputs copied from pinned host
-memory and the outputs copied back, inside the timed region.
+memory and the outputs copied back, inside the timed region. Decode takes
+its host buffers through gdn_forward_host (the kernel reads the pinned host
+inputs and writes the pinned host outputs over the host link itself, all on
+the launch stream), with the copy-engine pipeline (copies on their own
+streams, overlapping neighbouring calls) reported beside it; the other
+workloads use the copy-engine pipeline.
 
 --impl reference times the fp64 CPU oracle (a deliberately slow baseline) on
 the same workload, on this host's cores, on a bounded sample per step.
@@ -41,6 +46,12 @@ from gated_delta_net_02_gb300 import inputs  # noqa: E402
 
 METRIC = "GDN tokens/s (decode, verify, prefill); % of HBM GB/s or tensor peak"
 FALLBACK_HBM_GBS = 6800.0
+E2E_HOST_PATH = ("gdn_forward_host: each call reads its step's inputs from pinned host "
+                 "memory and writes its output to pinned host memory over the host link "
+                 "itself, one stream, no copy engine")
+E2E_COPY_PATH = ("gdn_forward(_chunked) on device buffers: one pinned host-to-device copy "
+                 "per step on a copy-in stream, one device-to-host copy of the output on a "
+                 "copy-out stream, overlapping the neighbouring steps' calls")
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -237,6 +248,11 @@ class PackedInputs:
         self.stage[b].copy_(self.host[p], non_blocking=True)
         return self.views[b]
 
+    def host_views(self, p):
+        """Typed views of host step p itself (pinned, for gdn_forward_host)."""
+        return [self.host[p, o:o + nb].view(v.dtype).view(v.shape)
+                for v, o, nb in zip(self.views[0], self.offs, self.nbytes)]
+
 
 class E2EPipeline:
     """End-to-end steps with the copies of neighbouring steps overlapping:
@@ -285,6 +301,28 @@ class E2EPipeline:
             if self.used[b]:
                 stream.wait_event(self.ev_out[b])
                 stream.wait_event(self.ev_in[b])
+
+
+class HostIOPipeline:
+    """End-to-end steps through gdn_forward_host: the call of step i reads
+    that step's inputs straight from its slice of the pinned host pool and
+    writes its output into pinned host buffer i % 2, over the host link, on
+    the launch stream; no copy-engine transfer and no cross-stream event
+    between consecutive calls."""
+
+    def __init__(self, wl, dev):
+        self.wl = wl
+        self.views = [wl.packed.host_views(p) for p in range(wl.packed.host.shape[0])]
+
+    def begin(self, stream):
+        pass
+
+    def step(self, i, stream):
+        wl = self.wl
+        wl.e2e_call_host(i, self.views[wl.e2e_host_index(i)], wl.out_host2[i % 2], stream)
+
+    def end(self, stream):
+        pass
 
 
 class Decode:
@@ -364,6 +402,12 @@ class Decode:
         q, k, v, g, beta = views
         src, dst = self._bufs(i)
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, src, dst, out, 1, "gda", stream)
+
+    def e2e_call_host(self, i, views, out, stream):
+        q, k, v, g, beta = views
+        src, dst = self._bufs(i)
+        self.gdn.gdn_forward_host(self.shape, q, k, v, g, beta, src, dst, out, 1, "gda",
+                                  stream)
 
     def graph_len(self):
         return self.POOL  # a multiple of 2 x SETS: replays continue every chain
@@ -455,6 +499,12 @@ class Verify(Decode):
         q, k, v, g, beta = views
         self.gdn.gdn_forward(self.shape, q, k, v, g, beta, self.bank_ptrs[i % self.BANKS],
                              self.slots, out, self.K, "gda", stream)
+
+    # No e2e_call_host: a verify call's 3.2 MB of tokens would cross the host
+    # link at the start of every CTA, ahead of its compute (4.07 M tokens/s
+    # end to end, measured), while copy-engine transfers of the next call's
+    # tokens overlap this call (4.64 M tokens/s).
+    e2e_call_host = None
 
     def graph_len(self):
         return self.POOL
@@ -834,21 +884,26 @@ def measure(wl, args, gdn, dev, stream, ws, rank, local):
     gdn.gdn_check_device_error(stream)
     del graphs
 
-    # e2e: host inputs in, host outputs back, every step, same K; the copies
-    # of neighbouring steps overlap each call (E2EPipeline), within graphs of
-    # at least 16 steps
-    pipe = E2EPipeline(wl, dev)
-    graphs_e2e = graphs_for(pipe.step, max(L, min(K, 16)), lambda: pipe.begin(stream),
-                            lambda: pipe.end(stream))
-    with torch.cuda.stream(stream):
-        for g, _ in graphs_e2e:
-            g.replay()
-    stream.synchronize()
-    barrier()
-    ms_e2e = timed_graph_steps(graphs_e2e, K, stream)
-    barrier()
-    gdn.gdn_check_device_error(stream)
-    del graphs_e2e
+    # e2e: host inputs in, host outputs back, every step, same K, within
+    # graphs of at least 16 steps: through gdn_forward_host where the
+    # workload has it (HostIOPipeline), and with copy-engine transfers whose
+    # neighbouring steps overlap each call (E2EPipeline)
+    def time_e2e(pipe):
+        graphs_e2e = graphs_for(pipe.step, max(L, min(K, 16)), lambda: pipe.begin(stream),
+                                lambda: pipe.end(stream))
+        with torch.cuda.stream(stream):
+            for g, _ in graphs_e2e:
+                g.replay()
+        stream.synchronize()
+        barrier()
+        t = timed_graph_steps(graphs_e2e, K, stream)
+        barrier()
+        gdn.gdn_check_device_error(stream)
+        del graphs_e2e
+        return t
+
+    ms_e2e_copy = time_e2e(E2EPipeline(wl, dev))
+    ms_e2e = time_e2e(HostIOPipeline(wl, dev)) if getattr(wl, "e2e_call_host", None) else None
 
     in_place = None
     if wl.name == "decode" and K >= L:
@@ -867,7 +922,7 @@ def measure(wl, args, gdn, dev, stream, ws, rank, local):
                     "note": "one 64-sequence batch stepping in place: its 64 MiB state "
                             "ping-pongs between two buffers and largely stays in L2; an L2 "
                             "figure beside the cold-L2 headline, not the headline"}
-    return ms, ms_e2e, in_place, summarize_clocks(clock_rows, t_wall0, t_wall1)
+    return ms, ms_e2e, ms_e2e_copy, in_place, summarize_clocks(clock_rows, t_wall0, t_wall1)
 
 
 def roofline(wl, kern_s):
@@ -925,9 +980,13 @@ def gdn_arm(args, names):
         wl = WORKLOADS[name]()
         wl.setup(gdn, dev)
         torch.cuda.synchronize()
-        ms, ms_e2e, in_place, clocks = measure(wl, args, gdn, dev, stream, ws, rank, local)
+        ms, ms_e2e, ms_e2e_copy, in_place, clocks = measure(wl, args, gdn, dev, stream, ws,
+                                                            rank, local)
+        host_io = ms_e2e is not None
         ms_max, ms_e2e_max, value, e2e_value = aggregate_over_ranks(
-            ms, ms_e2e, wl.tokens_per_step, K, ws, dev)
+            ms, ms_e2e if host_io else ms_e2e_copy, wl.tokens_per_step, K, ws, dev)
+        _, _, _, e2e_copy_value = aggregate_over_ranks(
+            ms, ms_e2e_copy, wl.tokens_per_step, K, ws, dev)
         line = None
         if rank == 0:
             kern_s = ms / K / 1e3  # this rank's average launch duration
@@ -939,7 +998,11 @@ def gdn_arm(args, names):
                 "roofline": roofline(wl, kern_s),
                 "e2e": {"value": e2e_value, "unit": "tokens/s",
                         "h2d_bytes_per_step": wl.h2d_bytes,
-                        "d2h_bytes_per_step": wl.d2h_bytes},
+                        "d2h_bytes_per_step": wl.d2h_bytes,
+                        "ms_per_step": ms_e2e_max / K,
+                        "path": E2E_HOST_PATH if host_io else E2E_COPY_PATH,
+                        **({"copy_engine": {"value": e2e_copy_value, "unit": "tokens/s",
+                                            "path": E2E_COPY_PATH}} if host_io else {})},
                 "gpu_launches": K * wl.launches_per_step(),
                 **({"l2_warm_in_place": in_place} if in_place else {}),
                 "clocks": clocks,

@@ -18,6 +18,7 @@ namespace {
 
 thread_local std::string g_msg;
 
+__attribute__((format(printf, 2, 3))) gdn_status fail(gdn_status st, const char *fmt, ...);
 gdn_status fail(gdn_status st, const char *fmt, ...) {
   char buf[512];
   va_list ap;
@@ -91,46 +92,67 @@ static gdn_status qk_heads(const char *fn, int H, int H_qk, int qk_map, int *hq)
   return GDN_OK;
 }
 
-gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
-                       const void *v, const float *g, const float *beta,
-                       const float *const *state_in, float *state_slots,
-                       float *out, int n_slots, gdn_mode mode,
-                       gdn_stream_t stream) {
-  if (!shape) return fail(GDN_ERR_INVALID_ARG, "gdn_forward: shape is NULL");
+// True when the device can dereference p: device or managed memory, or
+// page-locked host memory mapped into the device's address space at the same
+// address (unified addressing). Pageable host memory is refused.
+static bool device_reachable(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error the query reported
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeHost && at.devicePointer == p;
+}
+
+// gdn_forward and gdn_forward_host: the same checks and kernel arithmetic;
+// host_io reads the token rows with ordinary loads (host memory allowed).
+static gdn_status forward_impl(const char *fn, const gdn_shape *shape, const void *q,
+                               const void *k, const void *v, const float *g,
+                               const float *beta, const float *const *state_in,
+                               float *state_slots, float *out, int n_slots, gdn_mode mode,
+                               gdn_stream_t stream, bool host_io) {
+  if (!shape) return fail(GDN_ERR_INVALID_ARG, "%s: shape is NULL", fn);
   const gdn_shape &s = *shape;
   if (s.n_seqs < 0 || s.T < 0 || s.H <= 0)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: n_seqs=%d T=%d H=%d", s.n_seqs, s.T, s.H);
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs=%d T=%d H=%d", fn, s.n_seqs, s.T, s.H);
   if (mode != GDN_MODE_GDA && mode != GDN_MODE_KDA)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: mode %d", (int)mode);
+    return fail(GDN_ERR_INVALID_ARG, "%s: mode %d", fn, (int)mode);
   if (s.in_dtype != GDN_F32 && s.in_dtype != GDN_BF16)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: in_dtype %d", (int)s.in_dtype);
+    return fail(GDN_ERR_INVALID_ARG, "%s: in_dtype %d", fn, (int)s.in_dtype);
   if (n_slots < 1)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: n_slots=%d (need >= 1)", n_slots);
+    return fail(GDN_ERR_INVALID_ARG, "%s: n_slots=%d (need >= 1)", fn, n_slots);
   if (s.D_k <= 0 || s.D_v <= 0)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: D_k=%d D_v=%d", s.D_k, s.D_v);
+    return fail(GDN_ERR_INVALID_ARG, "%s: D_k=%d D_v=%d", fn, s.D_k, s.D_v);
   if (!head_size_ok(s.D_k) || !head_size_ok(s.D_v))
-    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward: head sizes D_k=%d D_v=%d (supported: 64, 128)",
+    return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes D_k=%d D_v=%d (supported: 64, 128)", fn,
                 s.D_k, s.D_v);
   if (!std::isfinite(s.scale))
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: scale is not finite");
+    return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
   int hq = 0;
-  if (qk_heads("gdn_forward", s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
+  if (qk_heads(fn, s.H, s.H_qk, (int)s.qk_map, &hq) != GDN_OK) return GDN_ERR_INVALID_ARG;
   const long long ntok = (long long)s.n_seqs * s.T;
   if (ntok > (1LL << 31) / s.H)
-    return fail(GDN_ERR_UNSUPPORTED, "gdn_forward: %lld tokens x %d heads too large", ntok, s.H);
+    return fail(GDN_ERR_UNSUPPORTED, "%s: %lld tokens x %d heads too large", fn, ntok, s.H);
   if (s.n_seqs == 0) return ok();
   if (!state_in || !state_slots)
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: state_in/state_slots is NULL");
+    return fail(GDN_ERR_INVALID_ARG, "%s: state_in/state_slots is NULL", fn);
   if (!aligned16(state_in) || !aligned16(state_slots))
-    return fail(GDN_ERR_INVALID_ARG, "gdn_forward: state buffers must be 16-byte aligned");
+    return fail(GDN_ERR_INVALID_ARG, "%s: state buffers must be 16-byte aligned", fn);
   if (ntok == 0) return ok();
   const void *ptrs[] = {q, k, v, g, beta, out};
   const char *names[] = {"q", "k", "v", "g", "beta", "out"};
   for (int i = 0; i < 6; ++i) {
-    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "gdn_forward: %s is NULL", names[i]);
+    if (!ptrs[i]) return fail(GDN_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
     if (!aligned16(ptrs[i]))
-      return fail(GDN_ERR_INVALID_ARG, "gdn_forward: %s is not 16-byte aligned", names[i]);
+      return fail(GDN_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, names[i]);
   }
+  if (host_io)
+    for (int i = 0; i < 6; ++i)
+      if (!device_reachable(ptrs[i]))
+        return fail(GDN_ERR_INVALID_ARG,
+                    "%s: %s is neither device memory nor page-locked host memory mapped at "
+                    "the same address", fn, names[i]);
   int *err = nullptr;
   gdn_status st = device_err_ptr(&err);
   if (st != GDN_OK) return st;
@@ -147,8 +169,27 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
   a.scale = s.scale != 0.f ? s.scale : 1.0f / std::sqrt((float)s.D_k);
   a.err = err;
   a.pdl = true;  // prologue overlaps the previous kernel of the stream
+  a.host_io = host_io;
   return check_launch(gdn::launch_recurrent(a, reinterpret_cast<cudaStream_t>(stream)),
-                      "gdn_forward launch");
+                      host_io ? "gdn_forward_host launch" : "gdn_forward launch");
+}
+
+gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
+                       const void *v, const float *g, const float *beta,
+                       const float *const *state_in, float *state_slots,
+                       float *out, int n_slots, gdn_mode mode,
+                       gdn_stream_t stream) {
+  return forward_impl("gdn_forward", shape, q, k, v, g, beta, state_in, state_slots, out,
+                      n_slots, mode, stream, false);
+}
+
+gdn_status gdn_forward_host(const gdn_shape *shape, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            const float *const *state_in, float *state_slots,
+                            float *out, int n_slots, gdn_mode mode,
+                            gdn_stream_t stream) {
+  return forward_impl("gdn_forward_host", shape, q, k, v, g, beta, state_in, state_slots,
+                      out, n_slots, mode, stream, true);
 }
 
 size_t gdn_chunked_workspace_size(const gdn_varlen_shape *shape, int n_slots) {

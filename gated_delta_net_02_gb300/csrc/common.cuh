@@ -160,6 +160,17 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
   return r;
 }
 
+// Ordinary 16-byte load, issued where it stands (volatile, so that it is not
+// moved behind later loads); page-locked host memory mapped into the
+// device's address space is read this way too.
+__device__ __forceinline__ uint4 ld_u4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ void st_f4(float *p, float4 v) {
   asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x),
                "f"(v.y), "f"(v.z), "f"(v.w)

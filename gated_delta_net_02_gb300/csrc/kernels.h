@@ -35,6 +35,10 @@ struct RecurrentArgs {
   // heads with fp32 inputs take a narrower slice per CTA (16 lanes across
   // the key rows, 32 columns), which shortens each token's step
   bool long_chains = false;
+  // q, k, v, g, beta and out may be page-locked host memory (mapped into the
+  // device's address space): the token tiles are read with ordinary loads,
+  // not bulk copies (gdn_forward_host); requires pdl
+  bool host_io = false;
 };
 
 cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream);

@@ -44,6 +44,7 @@ struct RecParams {
   float *ckpt;          // optional checkpoints, [n_seqs][max_ckpts][H][Dk][Dv]
   int pdl;              // launched programmatically (tok_start, seq_len, ckpt NULL)
   int long_chains;      // see RecurrentArgs
+  int host_io;          // see RecurrentArgs
   const int *pos0;      // position of each sequence's first token (NULL = 0)
   int ckpt_every, max_ckpts;
   float scale;
@@ -72,6 +73,13 @@ struct RecCfg {
   static constexpr int F_ALPHA = KDA ? DK : 1;
   static constexpr int F_FLOATS = TT * (2 * DK + CCOLS + F_ALPHA + 1);
   static constexpr size_t SMEM = 2 * RAW_BYTES + F_FLOATS * 4 + 64;
+  // 16-byte pieces of one token's raw rows (q, k, v, then the KDA gates) and
+  // of a whole tile per thread, when the tile is read with ordinary loads
+  static constexpr int P_QK = DK * (int)sizeof(Tin) / 16;
+  static constexpr int P_V = CCOLS * (int)sizeof(Tin) / 16;
+  static constexpr int P_G = KDA ? DK * 4 / 16 : 0;
+  static constexpr int P_TOK = 2 * P_QK + P_V + P_G;
+  static constexpr int P_THREAD = (TT * P_TOK + NT - 1) / NT;
   static_assert(ROWG * CG == 32, "lane split");
   static_assert(DK % ROWG == 0 && DV % CCOLS == 0, "shape split");
   static_assert(RAW_QK % 16 == 0 && RAW_V % 16 == 0, "bulk copy alignment");
@@ -134,9 +142,12 @@ __device__ __forceinline__ float4 token_update(float4 (&st)[C::RPT], const float
 }
 
 // CKPT: also store the checkpoints of p.ckpt (a separate instance, so the
-// decode and verify instances carry no trace of it)
-template <class C, bool CKPT>
-__global__ void __launch_bounds__(C::NT)
+// decode and verify instances carry no trace of it). HOSTIO: the token tiles
+// are read with ordinary loads instead of bulk copies, so q, k, v, g, beta
+// (and out, always written with ordinary stores) may be page-locked host
+// memory mapped into the device's address space.
+template <class C, bool CKPT, bool HOSTIO = false>
+__global__ void __launch_bounds__(C::NT, HOSTIO ? 512 / C::NT : 0)
     recurrent_kernel(const RecParams p) {
   using Tin = typename C::Tin;
   constexpr int DK = C::DK, DV = C::DV, ROWG = C::ROWG, CG = C::CG;
@@ -207,6 +218,48 @@ __global__ void __launch_bounds__(C::NT)
                  DK * 4, &bar[b]);
     }
   };
+  // HOSTIO: the same raw layout, filled by 16-byte loads spread over the
+  // CTA (piece e: token e / P_TOK, then q, k, v and the KDA gates in turn).
+  // A tile's loads are issued into registers early (before the state loads
+  // for the first tile, before the previous tile's tokens otherwise) and
+  // stored to shared memory later, so that the latency of the host link
+  // overlaps other work.
+  uint4 hreg[HOSTIO ? C::P_THREAD : 1];
+  auto piece_dst = [&](int e) -> uint32_t {
+    const int r = e / C::P_TOK, c = e - r * C::P_TOK;
+    if (c < C::P_QK) return r * DK * (int)sizeof(Tin) + c * 16;
+    if (c < 2 * C::P_QK) return C::RAW_QK + r * DK * (int)sizeof(Tin) + (c - C::P_QK) * 16;
+    if (c < 2 * C::P_QK + C::P_V)
+      return 2 * C::RAW_QK + r * CCOLS * (int)sizeof(Tin) + (c - 2 * C::P_QK) * 16;
+    return 2 * C::RAW_QK + C::RAW_V + r * DK * 4 + (c - 2 * C::P_QK - C::P_V) * 16;
+  };
+  auto piece_src = [&](int tile, int e) -> const void * {
+    const int r = e / C::P_TOK, c = e - r * C::P_TOK;
+    const long long tok = t0 + tile * TT + r;
+    const long long row = tok * p.H + h, row_qk = tok * p.Hqk + hq;
+    if (c < C::P_QK) return reinterpret_cast<const uint4 *>(q + row_qk * DK) + c;
+    if (c < 2 * C::P_QK) return reinterpret_cast<const uint4 *>(k + row_qk * DK) + (c - C::P_QK);
+    if (c < 2 * C::P_QK + C::P_V)
+      return reinterpret_cast<const uint4 *>(v + row * DV + col_base) + (c - 2 * C::P_QK);
+    return reinterpret_cast<const uint4 *>(p.g + row * DK) + (c - 2 * C::P_QK - C::P_V);
+  };
+  auto host_load = [&](int tile) {
+    const int np = min(TT, T_s - tile * TT) * C::P_TOK;
+#pragma unroll
+    for (int j = 0; j < C::P_THREAD; ++j) {
+      const int e = tid + j * C::NT;
+      if (e < np) hreg[j] = ld_u4(piece_src(tile, e));
+    }
+  };
+  auto host_store = [&](int tile, int b) {
+    const int np = min(TT, T_s - tile * TT) * C::P_TOK;
+    unsigned char *rb = smem + b * C::RAW_BYTES;
+#pragma unroll
+    for (int j = 0; j < C::P_THREAD; ++j) {
+      const int e = tid + j * C::NT;
+      if (e < np) *reinterpret_cast<uint4 *>(rb + piece_dst(e)) = hreg[j];
+    }
+  };
   // gate and beta scalars of a tile (the GDA gate is one value per token),
   // loaded into registers ahead of the tile's wait
   auto gate_scalars = [&](int tile, float &gv, float &bv) {
@@ -228,7 +281,8 @@ __global__ void __launch_bounds__(C::NT)
   // pointer array). Without a programmatic launch the wait returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // token copies and gate scalars first, then the state pointer
-  if (warp == 0) issue(0, 0);
+  if constexpr (HOSTIO) host_load(0);
+  else if (warp == 0) issue(0, 0);
   float g_cur, b_cur;
   gate_scalars(0, g_cur, b_cur);
 
@@ -239,7 +293,7 @@ __global__ void __launch_bounds__(C::NT)
     if (a < hi && b > lo) {  // overlaps the slot buffer: refuse this sequence
       if (tid == 0) {
         set_error(p.err, kDevOverlap);
-        mbar_wait(&bar[0], 0, nullptr);  // the first tile's copies land before exit
+        if (!HOSTIO) mbar_wait(&bar[0], 0, nullptr);  // the first tile's copies land before exit
       }
       return;
     }
@@ -256,6 +310,7 @@ __global__ void __launch_bounds__(C::NT)
 #pragma unroll
     for (int m = 0; m < RPT; ++m) st[m] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if constexpr (HOSTIO) host_store(0, 0);
 
   const int first_snap = T_s - p.n_slots;  // tokens t >= first_snap are stored
   int pos0 = 0;
@@ -267,10 +322,14 @@ __global__ void __launch_bounds__(C::NT)
     const int b = tile & 1;
     const uint32_t parity = (tile >> 1) & 1;
     const int n = min(TT, T_s - tile * TT);
-    if (warp == 0 && tile + 1 < ntiles) issue(tile + 1, b ^ 1);
+    if constexpr (HOSTIO) {
+      if (tile + 1 < ntiles) host_load(tile + 1);
+    } else if (warp == 0 && tile + 1 < ntiles) {
+      issue(tile + 1, b ^ 1);
+    }
     float g_nxt = 0.f, b_nxt = 0.f;
     if (tile + 1 < ntiles) gate_scalars(tile + 1, g_nxt, b_nxt);
-    if (tid == 0 && !mbar_wait(&bar[b], parity, p.err, kSiteRecTile)) abort_flag = 1;
+    if (!HOSTIO && tid == 0 && !mbar_wait(&bar[b], parity, p.err, kSiteRecTile)) abort_flag = 1;
     if (tid < n) {
       if constexpr (!C::KDA) fa[tid] = expf(g_cur);
       fb[tid] = b_cur;
@@ -280,7 +339,8 @@ __global__ void __launch_bounds__(C::NT)
     __syncthreads();
     if (abort_flag) {
       // Let a copy still in flight for the next tile land before exiting.
-      if (tid == 0 && tile + 1 < ntiles) mbar_wait(&bar[b ^ 1], ((tile + 1) >> 1) & 1, nullptr);
+      if (!HOSTIO && tid == 0 && tile + 1 < ntiles)
+        mbar_wait(&bar[b ^ 1], ((tile + 1) >> 1) & 1, nullptr);
       return;
     }
     {  // convert the raw tile to fp32
@@ -334,6 +394,9 @@ __global__ void __launch_bounds__(C::NT)
         }
       }
     }
+    if constexpr (HOSTIO) {
+      if (tile + 1 < ntiles) host_store(tile + 1, b ^ 1);
+    }
     __syncthreads();  // fp32 tile buffers are rewritten by the next tile
   }
 }
@@ -374,8 +437,27 @@ cudaError_t launch_t(const RecParams &p, cudaStream_t stream) {
   return launch_c<typename RecPick<DK, DV, KDA, Tin>::C>(p, stream);
 }
 
+// gdn_forward_host: the configuration of gdn_forward (same arithmetic), with
+// the token tiles read by ordinary loads; a programmatic launch like it.
+template <int DK, int DV, bool KDA, typename Tin>
+cudaError_t launch_host_io(const RecParams &p, cudaStream_t stream) {
+  using C = typename RecPick<DK, DV, KDA, Tin>::C;
+  const long long n_items = (long long)p.n_seqs * p.H * C::CTAS_PER_HEAD;
+  if (n_items == 0) return cudaSuccess;
+  if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(recurrent_kernel<C, false, true>, dim3((unsigned)n_items), dim3(C::NT),
+                    C::SMEM, stream, p);
+}
+
 template <int DK, int DV>
 cudaError_t launch_d(const RecParams &p, bool kda, bool bf16, cudaStream_t s) {
+  if (p.host_io) {
+    if (kda)
+      return bf16 ? launch_host_io<DK, DV, true, __nv_bfloat16>(p, s)
+                  : launch_host_io<DK, DV, true, float>(p, s);
+    return bf16 ? launch_host_io<DK, DV, false, __nv_bfloat16>(p, s)
+                : launch_host_io<DK, DV, false, float>(p, s);
+  }
   if constexpr (DK == 128 && DV == 128) {
     // long fp32 chains: a token's step is latency-bound, and a narrower slice
     // per CTA shortens it (about 10% on the varlen fp32 prefill)
@@ -404,6 +486,7 @@ cudaError_t launch_recurrent(const RecurrentArgs &a, cudaStream_t stream) {
   p.ckpt = a.ckpt; p.pos0 = a.pos0;
   p.pdl = a.pdl && !a.tok_start && !a.seq_len && !a.ckpt ? 1 : 0;
   p.long_chains = a.long_chains ? 1 : 0;
+  p.host_io = a.host_io && p.pdl ? 1 : 0;
   p.ckpt_every = a.ckpt_every > 0 ? a.ckpt_every : 1; p.max_ckpts = a.max_ckpts;
   p.scale = a.scale; p.err = a.err;
   if (a.Dk == 128 && a.Dv == 128) return launch_d<128, 128>(p, a.kda, a.bf16, stream);

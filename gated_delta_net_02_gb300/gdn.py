@@ -68,6 +68,8 @@ lib.gdn_version.restype = ctypes.c_char_p
 lib.gdn_forward.restype = _st
 lib.gdn_forward.argtypes = [ctypes.POINTER(gdn_shape), _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _i, _i, _vp]
+lib.gdn_forward_host.restype = _st
+lib.gdn_forward_host.argtypes = lib.gdn_forward.argtypes
 lib.gdn_chunked_workspace_size.restype = ctypes.c_size_t
 lib.gdn_chunked_workspace_size.argtypes = [ctypes.POINTER(gdn_varlen_shape), _i]
 lib.gdn_forward_chunked.restype = _st
@@ -147,6 +149,15 @@ def gdn_forward(shape: gdn_shape, q, k, v, g, beta, state_in, state_slots, out,
     _check(lib.gdn_forward(ctypes.byref(shape), _addr(q), _addr(k), _addr(v), _addr(g),
                            _addr(beta), _addr(state_in), _addr(state_slots), _addr(out),
                            int(n_slots), _MODES[mode], _stream(stream)))
+
+
+def gdn_forward_host(shape: gdn_shape, q, k, v, g, beta, state_in, state_slots, out,
+                     n_slots: int, mode, stream=None) -> None:
+    """gdn_forward whose q, k, v, g, beta and out may be pinned host tensors
+    (or device tensors): the kernel reads and writes them over the host link."""
+    _check(lib.gdn_forward_host(ctypes.byref(shape), _addr(q), _addr(k), _addr(v), _addr(g),
+                                _addr(beta), _addr(state_in), _addr(state_slots), _addr(out),
+                                int(n_slots), _MODES[mode], _stream(stream)))
 
 
 def gdn_chunked_workspace_size(shape: gdn_varlen_shape, n_slots: int) -> int:

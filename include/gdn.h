@@ -126,6 +126,27 @@ gdn_status gdn_forward(const gdn_shape *shape, const void *q, const void *k,
                        float *out, int n_slots, gdn_mode mode,
                        gdn_stream_t stream);
 
+/*
+ * gdn_forward with the per-token buffers in host memory (no counterpart on
+ * the pages): q, k, v, g, beta and out may each be page-locked host memory
+ * (cudaMallocHost / cudaHostAlloc / cudaHostRegister, mapped into the
+ * device's address space at the same address, as unified addressing does)
+ * or device memory. The kernel reads the token rows and writes the outputs
+ * over the host link itself, so no separate copy (and no event between a copy
+ * stream and the launch stream) stands between consecutive calls; the state
+ * pointers and slots stay device memory. Layouts, results (bit for bit) and
+ * the programmatic launch are those of gdn_forward.
+ * Errors: GDN_ERR_INVALID_ARG when one of the six pointers is pageable host
+ * memory or unknown to CUDA (each is checked with cudaPointerGetAttributes
+ * before anything is enqueued), otherwise as gdn_forward. The host memory
+ * must stay valid and unmodified until the call has completed on `stream`.
+ */
+gdn_status gdn_forward_host(const gdn_shape *shape, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            const float *const *state_in, float *state_slots,
+                            float *out, int n_slots, gdn_mode mode,
+                            gdn_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Varlen chunked prefill ("llama : enable chunked fused GDN path", llama.cpp
  * commits, tag b9752). Sequence s covers packed tokens

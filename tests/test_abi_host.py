@@ -75,6 +75,33 @@ def test_forward_argument_errors(gdn):
     assert "mode" in gdn.gdn_last_error()
 
 
+def test_forward_host_argument_errors(gdn):
+    """gdn_forward_host makes gdn_forward's checks (under its own name), then
+    refuses a pointer CUDA does not know as device or page-locked host memory
+    before anything is enqueued (here: an address nothing allocated)."""
+    def call(sh, n_slots=1, **ptrs):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=FAKE, state_slots=FAKE,
+                 out=FAKE)
+        p.update(ptrs)
+        with pytest.raises(gdn.GDNError) as e:
+            gdn.gdn_forward_host(sh, p["q"], p["k"], p["v"], p["g"], p["beta"], p["state_in"],
+                                 p["state_slots"], p["out"], n_slots, "gda")
+        return e.value.status, gdn.gdn_last_error()
+
+    assert call(shape(gdn, D_k=32))[0] == gdn.GDN_ERR_UNSUPPORTED
+    st, msg = call(shape(gdn), n_slots=0)
+    assert st == gdn.GDN_ERR_INVALID_ARG and msg.startswith("gdn_forward_host: n_slots")
+    st, msg = call(shape(gdn), beta=FAKE + 4)
+    assert st == gdn.GDN_ERR_INVALID_ARG and "beta is not 16-byte aligned" in msg
+    st, msg = call(shape(gdn))
+    assert st == gdn.GDN_ERR_INVALID_ARG
+    assert msg == ("gdn_forward_host: q is neither device memory nor page-locked host "
+                   "memory mapped at the same address")
+    assert gdn.lib.gdn_forward_host(None, 0, 0, 0, 0, 0, 0, 0, 0, 1, 0, None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    gdn.gdn_forward_host(shape(gdn, n_seqs=0), 0, 0, 0, 0, 0, 0, 0, 0, 1, "gda")
+
+
 def test_null_shape(gdn):
     assert gdn.lib.gdn_forward(None, 0, 0, 0, 0, 0, 0, 0, 0, 1, 0, None) == gdn.GDN_ERR_INVALID_ARG
 
