@@ -972,21 +972,27 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
 //
 // One CTA per (sequence, head, half of the value columns): NV = 64 state
 // columns, all chunks of the sequence in order. Roles:
-//   warps 0-7 "state": thread (key row i = 32 (w & 3) + lane, 32 columns
-//             32 (w >> 2)..) owns that part of the fp32 state; turns X into
-//             D and D~, applies the state update, writes outputs;
-//   warp 8    "producer": TMA loads of each chunk's tiles into a two-stage
-//             ring (and zero padding rows of a partial last chunk);
-//   warp 9    "mma": lane 0 issues every tcgen05.mma.
+//   warps 0..STATE_WARPS-1 "state": thread (key row i = 32 (w & 3) + lane,
+//             CPT columns from CPT (w >> 2)) owns that part of the fp32
+//             state; turns X into D and D~, applies the state update, writes
+//             outputs (a warp reads TMEM lanes 32 (w & 3) .. + 31 only);
+//   warp STATE_WARPS "producer": TMA loads of each chunk's tiles into a
+//             two-stage ring (and zero padding rows of a partial last chunk);
+//   warp STATE_WARPS + 1 "mma": lane 0 issues every tcgen05.mma.
 // Per chunk the state-dependent chain is: X += [-W; Q] S0 (mma) -> D (state)
 // -> S_acc = K~^T D~ (mma) -> S = e^gC . S0 + S_acc (state) -> next chunk.
 // Off that chain: [T; 0] V of the next chunk is issued right behind the
 // state update, [0; P] D right behind the next chunk's [-W; Q] S0, and the
 // outputs of a chunk are stored while the next chunk's state update runs.
 constexpr int NV = 64;
-constexpr int STATE_THREADS = 256;
-constexpr int SCAN_WARPS = 10;
+constexpr int STATE_WARPS = 8;  // a multiple of 4 (one warp per TMEM lane quadrant)
+constexpr int STATE_THREADS = 32 * STATE_WARPS;
+constexpr int PRODUCER_WARP = STATE_WARPS, MMA_WARP = STATE_WARPS + 1;
+constexpr int SCAN_WARPS = STATE_WARPS + 2;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32;
+// state columns per state thread (of the CTA's NV) and their 8-column pieces
+constexpr int CPT = NV / (STATE_WARPS / 4), PPT = CPT / 8;
+static_assert(STATE_WARPS % 4 == 0 && (CPT == 16 || CPT == 32), "state split");
 // stage: K (GDA) or K~ (KDA) [64 r][128 i] | [-W; Q or Q^] [128][128 i] |
 //        V [64 j][64 v] | T [64 r][64 j] | zeros [64][64] | P [64 r][64 j] |
 //        gate factors fp32 [256]
@@ -1008,7 +1014,14 @@ constexpr uint32_t COL_X0 = 0, COL_S = 192, COL_O0 = 256;
 // polls of the clean-up waits before exit (a healthy one ends at once)
 constexpr uint32_t kDrainPolls = 1u << 22;
 
-// Barrier over the 256 state threads (id 1). The non-aligned form counts
+// TMEM -> registers, CPT consecutive columns of the thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cpt(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 32) tmem_ld32(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+
+// Barrier over the state threads (id 1). The non-aligned form counts
 // threads, so lanes that reach it at different times are fine; __syncwarp
 // first reconverges the warp after a single-lane wait.
 __device__ __forceinline__ void named_bar(int id) {
@@ -1050,6 +1063,31 @@ __device__ __forceinline__ void store_rows32(float (&x)[32], float *dst, long lo
     *reinterpret_cast<float4 *>(dst + (long long)(8 * g + u) * ld + 4 * p) =
         make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
   transpose8x8(x, lane);
+}
+
+// Stores the 32 x 16 fp32 block a warp holds (lane l: row l, 16 consecutive
+// floats) to rows `ld` floats apart starting at dst: after a 4 x 4 transpose
+// of 16-byte pieces inside each group of 4 lanes, each store instruction
+// writes 64 contiguous bytes of 8 rows; a second transpose gives x back.
+__device__ __forceinline__ void store_rows16(float (&x)[16], float *dst, long long ld,
+                                             int lane) {
+  uint4 p[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    p[u] = make_uint4(__float_as_uint(x[4 * u]), __float_as_uint(x[4 * u + 1]),
+                      __float_as_uint(x[4 * u + 2]), __float_as_uint(x[4 * u + 3]));
+  transpose4x4(p, lane);
+  const int rb = lane & ~3, a = lane & 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<uint4 *>(dst + (long long)(rb + u) * ld + 4 * a) = p[u];
+}
+
+template <int N>
+__device__ __forceinline__ void store_rows_cpt(float (&x)[N], float *dst, long long ld,
+                                               int lane) {
+  if constexpr (N == 32) store_rows32(x, dst, ld, lane);
+  else store_rows16(x, dst, ld, lane);
 }
 
 // Bounded wait that also gives up early once another role has aborted. On
@@ -1182,7 +1220,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     reinterpret_cast<uint4 *>(sm + ST_Z)[e] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4 *>(sm + ST_BYTES + ST_Z)[e] = make_uint4(0, 0, 0, 0);
   }
-  if (warp == 9) {
+  if (warp == MMA_WARP) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -1192,7 +1230,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == 8) {
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     int issued = 0;
     if (lane == 0) {
@@ -1289,7 +1327,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
         drain_wait(&full[j & 1], (j >> 1) & 1);
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ mma
     if (lane == 0) {
       constexpr uint32_t id_x = idesc_bf16_f32(128, 64, false, true);
@@ -1377,27 +1415,28 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   } else {
     // ------------------------------------------------------------ state
     const int i = 32 * (warp & 3) + lane;  // key row / TMEM lane
-    const int ch = warp >> 2;              // which 32 of the CTA's 64 columns
+    const int ch = warp >> 2;              // which CPT of the CTA's 64 columns
+    const int c0 = CPT * ch;               // first of them
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     RoleSync rs{1, reinterpret_cast<int *>(sm + SC_RFLAGS), 0};
-    float Sm[32];
+    float Sm[CPT];
     {
       const float *src = state_in[s];
       if (src) {
         const float4 *p4 = reinterpret_cast<const float4 *>(
-            src + ((long long)h * DK + i) * DV + NV * vs + 32 * ch);
+            src + ((long long)h * DK + i) * DV + NV * vs + c0);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < CPT / 4; ++e) {
           const float4 v4 = p4[e];
           Sm[4 * e] = v4.x; Sm[4 * e + 1] = v4.y; Sm[4 * e + 2] = v4.z; Sm[4 * e + 3] = v4.w;
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) Sm[e] = 0.f;
+        for (int e = 0; e < CPT; ++e) Sm[e] = 0.f;
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, 4 * ch + q)) = pack8(Sm + 8 * q);
+      for (int q = 0; q < PPT; ++q)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, PPT * ch + q)) = pack8(Sm + 8 * q);
     }
     fence_proxy_async();
     named_bar(1);
@@ -1411,26 +1450,28 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       const int t0 = tok0 + CH * j, len = chunk_len_of(j);
       if ((warp & 3) >= 2) {
         const int r = i - CH;
-        float xv[32], ov[32];
-        tmem_ld32(tbase + lane_off + COL_X0 + 64u * (uint32_t)(j % 3) + 32 * ch, xv);
-        tmem_ld32(tbase + lane_off + COL_O0 + 64u * (uint32_t)(j & 1) + 32 * ch, ov);
-        float4 o4[8];
+        float xv[CPT], ov[CPT];
+        tmem_ld_cpt(tbase + lane_off + COL_X0 + 64u * (uint32_t)(j % 3) + c0, xv);
+        tmem_ld_cpt(tbase + lane_off + COL_O0 + 64u * (uint32_t)(j & 1) + c0, ov);
+        float4 o4[CPT / 4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < CPT / 4; ++u)
           o4[u] = make_float4(scale * fmaf(qf, xv[4 * u], ov[4 * u]),
                               scale * fmaf(qf, xv[4 * u + 1], ov[4 * u + 1]),
                               scale * fmaf(qf, xv[4 * u + 2], ov[4 * u + 2]),
                               scale * fmaf(qf, xv[4 * u + 3], ov[4 * u + 3]));
         if (len == CH) {
-          unsigned char *tile = sm + SC_OUT + ch * 8192 + r * 128;
+          // staging tile c0 / 32 (32 columns, 128-byte rows), pieces from (c0 % 32) / 4
+          unsigned char *tile = sm + SC_OUT + (c0 >> 5) * 8192 + r * 128;
+          const int pc0 = (c0 & 31) >> 2;
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<float4 *>(tile + ((u ^ (r & 7)) << 4)) = o4[u];
+          for (int u = 0; u < CPT / 4; ++u)
+            *reinterpret_cast<float4 *>(tile + (((pc0 + u) ^ (r & 7)) << 4)) = o4[u];
         } else if (r < len) {
           float4 *dst = reinterpret_cast<float4 *>(out + ((long long)(t0 + r) * H + h) * DV +
-                                                   NV * vs + 32 * ch);
+                                                   NV * vs + c0);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) dst[u] = o4[u];
+          for (int u = 0; u < CPT / 4; ++u) dst[u] = o4[u];
         }
       }
       if (len == CH) {
@@ -1460,18 +1501,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       }
       // D rows (TMEM lanes 0..63) -> D and D~ tiles
       if ((warp & 3) < 2) {
-        float dv[32];
-        tmem_ld32(tbase + lane_off + colx + 32 * ch, dv);
+        float dv[CPT];
+        tmem_ld_cpt(tbase + lane_off + colx + c0, dv);
         unsigned char *dbuf = sm + SC_D + (jc & 1) * 8192;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4 *>(dbuf + chunk16(i, 4 * ch + q)) = pack8(dv + 8 * q);
+        for (int q = 0; q < PPT; ++q)
+          *reinterpret_cast<uint4 *>(dbuf + chunk16(i, PPT * ch + q)) = pack8(dv + 8 * q);
         if constexpr (!KDA) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) dv[e] *= dec;
+          for (int e = 0; e < CPT; ++e) dv[e] *= dec;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4 *>(sm + SC_DT + chunk16(i, 4 * ch + q)) = pack8(dv + 8 * q);
+          for (int q = 0; q < PPT; ++q)
+            *reinterpret_cast<uint4 *>(sm + SC_DT + chunk16(i, PPT * ch + q)) =
+                pack8(dv + 8 * q);
         }
       }
       fence_proxy_async();
@@ -1482,14 +1524,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       if (!rs.wait(tid == 0, bE7, jc & 1, abort_flag, err, kSiteScanS, jc)) break;
       tc_fence_after();
       {
-        float v[32];
-        tmem_ld32(tbase + lane_off + COL_S + 32 * ch, v);
+        float v[CPT];
+        tmem_ld_cpt(tbase + lane_off + COL_S + c0, v);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) Sm[u] = fmaf(gcs, Sm[u], v[u]);
+        for (int u = 0; u < CPT; ++u) Sm[u] = fmaf(gcs, Sm[u], v[u]);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, 4 * ch + q)) = pack8(Sm + 8 * q);
+      for (int q = 0; q < PPT; ++q)
+        *reinterpret_cast<uint4 *>(sm + SC_S + chunk16(i, PPT * ch + q)) = pack8(Sm + 8 * q);
       fence_proxy_async();
       tc_fence_before();
       named_bar(1);
@@ -1499,10 +1541,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       if (CKPT && chunk_len_of(jc) == CH) {
         const int pos = (jc + 1) * CH, c = pos / ckpt_every - 1;
         if (pos % ckpt_every == 0 && c < max_ckpts)
-          store_rows32(Sm,
-                       ckpt + ((((long long)s * max_ckpts + c) * H + h) * DK + 32 * (warp & 3)) *
-                                  DV + NV * vs + 32 * ch,
-                       DV, lane);
+          store_rows_cpt(Sm,
+                         ckpt + ((((long long)s * max_ckpts + c) * H + h) * DK +
+                                 32 * (warp & 3)) * DV + NV * vs + c0,
+                         DV, lane);
       }
       // this chunk's outputs, while the next chunk's X is computed (the
       // staging tile is free once thread 0's earlier stores have read it)
@@ -1515,9 +1557,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
     if (tid == 0) bulk_wait_all();
     if (!*abort_flag) {  // state after the chunked part: read by the tail, or the slot itself
       float4 *dst = reinterpret_cast<float4 *>(
-          w.states + (((long long)s * H + h) * DK + i) * DV + NV * vs + 32 * ch);
+          w.states + (((long long)s * H + h) * DK + i) * DV + NV * vs + c0);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
+      for (int e = 0; e < CPT / 4; ++e)
         dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
     }
   }
@@ -1527,7 +1569,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   if (wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == MMA_WARP) {
     __syncwarp();
     tmem_dealloc(tbase, 512);
   }
