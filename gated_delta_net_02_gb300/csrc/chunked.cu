@@ -387,15 +387,14 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ntiles = w.hdr[0] * H;  // (chunks in use) x heads, chunk-major
   if ((int)blockIdx.x >= ntiles) return;
-  // Hand-off: the CTAs on about handoff_sms of the SMs take one tile each and
-  // leave, so that the scan's CTAs (one per SM) take those SMs while the rest
-  // of the prep goes on beside them.
-  bool one_tile = false;
+  // Hand-off: the CTAs on about handoff_sms of the SMs leave at once, so that
+  // the scan's CTAs (one per SM) take those SMs, set up and wait for their
+  // first tiles while the rest of the prep goes on beside them.
   if (handoff_sms > 0) {
     uint32_t smid, nsmid;
     asm("mov.u32 %0, %%smid;" : "=r"(smid));
     asm("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
-    one_tile = (long long)smid * num_sms < (long long)handoff_sms * nsmid;
+    if ((long long)smid * num_sms < (long long)handoff_sms * nsmid) return;
   }
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
@@ -527,7 +526,7 @@ __global__ void __launch_bounds__(PREP_THREADS, KDA ? 3 : 4)
     if (mbar_wait(bar_tma, par, err, kSitePrepLoad)) ++loads_done;
     else abort_flag = 1;
   }
-  if (tid == 64) s_claim[0] = one_tile ? ntiles : atomicAdd(&w.hdr[1], 1);
+  if (tid == 64) s_claim[0] = atomicAdd(&w.hdr[1], 1);
   __syncthreads();
   if constexpr (!KDA) {
     if (tid >= 32 && tid < CH) {
@@ -1069,8 +1068,8 @@ __device__ __forceinline__ void store_rows32(float (&x)[32], float *dst, long lo
 // floats) to rows `ld` floats apart starting at dst: after a 4 x 4 transpose
 // of 16-byte pieces inside each group of 4 lanes, each store instruction
 // writes 64 contiguous bytes of 8 rows; a second transpose gives x back.
-__device__ __forceinline__ void store_rows16(float (&x)[16], float *dst, long long ld,
-                                             int lane) {
+[[maybe_unused]] __device__ __forceinline__ void store_rows16(float (&x)[16], float *dst,
+                                                              long long ld, int lane) {
   uint4 p[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -1790,9 +1789,8 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     // The prep runs first, on every SM. When the scan (one CTA per SM) needs
     // at most half of the SMs, it is launched right behind the prep as a
     // programmatic dependent ("hand-off"): the prep CTAs on as many SMs as the
-    // scan has CTAs take one tile each and leave, the scan's CTAs take those
-    // SMs and wait for each tile's ready flag while the rest of the prep goes
-    // on. The scan can start only once every prep CTA has started, and the
+    // scan has CTAs leave at once, the scan's CTAs take those SMs and wait for
+    // each tile's ready flag while the rest of the prep goes on. The scan can start only once every prep CTA has started, and the
     // prep never waits on the scan, so the prep always finishes. With more
     // scan CTAs the prep left on the other SMs cannot keep up with the chains
     // (a schedule model with the measured rates puts the break-even between
