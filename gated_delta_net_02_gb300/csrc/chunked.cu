@@ -1172,8 +1172,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   // the prep is still running beside it: the work list is complete (every
   // prep CTA waited for it before this grid could start), and each chunk's
   // tiles are read only after their ready flags. Otherwise it waits for the
-  // whole prep here. The recurrent tail after it may start its own set-up
-  // now; it waits for this grid before reading the states.
+  // whole prep here. (The recurrent tail is launched normally and starts
+  // after this grid has completed.)
   if (!wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vs = blockIdx.x & 1;  // value-column half
@@ -1753,9 +1753,11 @@ cudaError_t launch_chunked(const ChunkedArgs &a, cudaStream_t stream) {
     // persistent prep CTAs: as many as fit at once (registers allow three per
     // SM for per-row gates, four for scalar gates; four use all of TMEM)
     const int per_sm = a.kda ? 3 : 4;
-    // Work list -> prep -> scan -> tail are programmatic dependent launches:
-    // each kernel's launch and set-up overlap the previous one's drain, and
-    // each waits (griddepcontrol.wait) before reading what that one wrote.
+    // The prep and the scan are programmatic dependent launches behind the
+    // work list: each one's launch and set-up overlap the previous kernel's
+    // drain, and each waits (griddepcontrol.wait) before reading what that
+    // one wrote. The work list and the recurrent tail are launched normally
+    // (programmatic launches of those two measured 4-5% slower).
     auto launch_prep = [&](int publish, int handoff) -> cudaError_t {
       const dim3 g3((unsigned)std::min<long long>(lay.max_chunks * a.H,
                                                   (long long)num_sms * per_sm));
