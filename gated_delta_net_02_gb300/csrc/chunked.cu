@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(WL_THREADS)
   __shared__ int bad;
   __shared__ int wsum[WL_THREADS / 32];
   __shared__ int scu[WL_SMEM_SEQS + 1];
+  __shared__ int sbase[WL_SMEM_SEQS + 1];  // first chunk of each sequence, then the count
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool in_smem = N <= WL_SMEM_SEQS;
   auto CU = [&](int i) { return in_smem ? scu[i] : cu[i]; };
@@ -302,14 +303,41 @@ __global__ void __launch_bounds__(WL_THREADS)
     w.tail_len[s] = L - Lc;
     w.tail_pos[s] = Lc;  // position of the first tail token within the sequence
     w.state_ptrs[s] = nch > 0 ? w.states + (long long)s * state_elems : state_in[s];
-    for (int j = 0; j < nch; ++j) {
-      w.chunk_seq[base + j] = s;
-      w.chunk_tok[base + j] = CU(s) + j * CH;
-      w.chunk_len[base + j] = min(CH, Lc - j * CH);
+    if (in_smem) {
+      sbase[s] = base;
+    } else {
+      for (int j = 0; j < nch; ++j) {
+        w.chunk_seq[base + j] = s;
+        w.chunk_tok[base + j] = CU(s) + j * CH;
+        w.chunk_len[base + j] = min(CH, Lc - j * CH);
+      }
     }
     base += nch;
   }
-  if (tid == WL_THREADS - 1) w.hdr[0] = incl;
+  if (tid == WL_THREADS - 1) {
+    w.hdr[0] = incl;
+    if (in_smem) sbase[N] = incl;
+  }
+  if (in_smem) {
+    // every thread fills chunks: chunk gc belongs to the last sequence whose
+    // first chunk is at most gc (sequences without chunks share their base
+    // with the next one)
+    __syncthreads();
+    const int nchunks = sbase[N];
+    for (int gc = tid; gc < nchunks; gc += WL_THREADS) {
+      int lo = 0, hi = N;  // sbase[lo] <= gc < sbase[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sbase[mid] <= gc) lo = mid;
+        else hi = mid;
+      }
+      const int j = gc - sbase[lo];
+      const int Lc = max(CU(lo + 1) - CU(lo) - K, 0);
+      w.chunk_seq[gc] = lo;
+      w.chunk_tok[gc] = CU(lo) + j * CH;
+      w.chunk_len[gc] = min(CH, Lc - j * CH);
+    }
+  }
   // longest chunk count first (ties by index); identity beyond 4096 sequences
   for (int s = tid; s < N; s += WL_THREADS) {
     if (N > 4096) {
