@@ -1196,13 +1196,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
                       int Hqk, int qk_grouped, float scale, WsPtrs w, float *ckpt,
                       int ckpt_every, int max_ckpts, int wait_ready, int *err) {
   constexpr int DK = 128, DV = 128;
-  // This grid is a programmatic dependent of the chunk prep. With wait_ready
-  // the prep is still running beside it: the work list is complete (every
-  // prep CTA waited for it before this grid could start), and each chunk's
-  // tiles are read only after their ready flags. Otherwise it waits for the
-  // whole prep here. (The recurrent tail is launched normally and starts
-  // after this grid has completed.)
-  if (!wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // This grid is a programmatic dependent of the chunk prep. The work list
+  // is complete when it starts (every prep CTA waited for it before this
+  // grid could start), and nothing here reads what the prep writes except
+  // the producer's copies of the prep's tiles: with wait_ready (the prep
+  // still running beside this grid) each chunk's tiles are copied only after
+  // their ready flags; otherwise the producer waits for the whole prep before
+  // its first copy, while the other roles set up. (The recurrent tail is
+  // launched normally and starts after this grid has completed.)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vs = blockIdx.x & 1;  // value-column half
   const int h = (blockIdx.x >> 1) % H;
@@ -1210,7 +1211,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
   const int s = w.order[(blockIdx.x >> 1) / H];
   const int nch = w.seq_nch[s];
   if (nch == 0) {
-    if (wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");  // see the end
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // see the end
     return;
   }
   const int chunk0 = w.seq_chunk0[s];
@@ -1268,6 +1269,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
       prefetch_tmap(&map_P);
       prefetch_tmap(&map_W);
     }
+    if (!wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int jc = 0; jc < nch; ++jc) {
       const int st = jc & 1;
       if (jc >= 2) {  // the products of chunk jc - 2 have released the stage
@@ -1590,10 +1592,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1)
         dst[e] = make_float4(Sm[4 * e], Sm[4 * e + 1], Sm[4 * e + 2], Sm[4 * e + 3]);
     }
   }
-  // Beside the prep, nothing else orders the prep's completion before this
-  // grid's: wait for it here (it has long finished), so that whatever runs
-  // after this grid in the stream finds the prep complete as well.
-  if (wait_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Only the producer may have waited for the prep so far (with wait_ready,
+  // nobody): every thread waits for it here (it has long finished), so that
+  // the grid's completion implies the prep's and whatever runs after this
+  // grid in the stream finds the prep complete as well.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {
