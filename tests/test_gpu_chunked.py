@@ -77,6 +77,20 @@ def test_varlen_ragged_small(gdn, mode):
     compare(b, out, slots)
 
 
+@pytest.mark.parametrize("n_seqs", [300, 4100])
+def test_many_sequences_work_list(gdn, n_seqs):
+    """Many short sequences (0 to 150 tokens: empty, shorter than K, one and
+    several chunks), H=1: 300 sequences (the work list keeps cu_seqlens in
+    shared memory and all its threads fill the chunk table) and 4100 (past its
+    shared-memory capacity: each thread fills its own sequences' chunks)"""
+    gen = np.random.default_rng(n_seqs)
+    lens = gen.integers(0, 151, n_seqs)
+    lens[:5] = [0, 64, 0, 0, 129]  # runs of empty sequences between chunked ones
+    b = inputs.make_batch(48, lens.tolist(), 1, 128, 128, mode="gda", n_slots=2)
+    out, slots = chunked_forward(gdn, b)
+    compare(b, out, slots)
+
+
 @pytest.mark.parametrize("mode", ["gda", "kda"])
 @pytest.mark.parametrize("K", [1, 8])
 def test_single_long_sequence(gdn, mode, K):
