@@ -145,7 +145,9 @@ __device__ __forceinline__ float4 token_update(float4 (&st)[C::RPT], const float
 // decode and verify instances carry no trace of it). HOSTIO: the token tiles
 // are read with ordinary loads instead of bulk copies, so q, k, v, g, beta
 // (and out, always written with ordinary stores) may be page-locked host
-// memory mapped into the device's address space.
+// memory mapped into the device's address space. The HOSTIO instance is
+// held to 512 threads' worth of CTAs per SM (the register budget the other
+// instances reach on their own); a minimum of 0 leaves those unbounded.
 template <class C, bool CKPT, bool HOSTIO = false>
 __global__ void __launch_bounds__(C::NT, HOSTIO ? 512 / C::NT : 0)
     recurrent_kernel(const RecParams p) {
