@@ -176,3 +176,35 @@ def test_host_calls_in_a_cuda_graph(gdn):
     for s in range(STEPS):
         assert torch.equal(outs_h[s].cuda(), outs_d[s]), s
     assert torch.equal(bank_h[STEPS % 2], bank_d[STEPS % 2])
+
+
+@pytest.mark.parametrize("T", [1, 12])
+def test_host_call_refuses_state_in_inside_slots(gdn, T):
+    """A state pointer into the slot buffer is refused by the device for that
+    sequence (GDN_ERR_DEVICE_ARG); the other sequence still runs and matches
+    the device-buffer call, and the error word clears."""
+    b = inputs.make_batch(15 + T, [T] * 2, 2, 128, 128, n_slots=2)
+    N, H = 2, 2
+    slots_h = torch.full((N, 2, H, 128, 128), float("nan"), device="cuda")
+    slots_d = slots_h.clone()
+    d = to_dev(b)
+    shape = gdn.gdn_shape(N, T, H, 128, 128, gdn.GDN_BF16, 0.0)
+    h = {n: getattr(b, n).contiguous().pin_memory() for n in NAMES}
+    out_h = torch.full((N * T, H, 128), float("nan")).pin_memory()
+    out_d = torch.full((N * T, H, 128), float("nan"), device="cuda")
+    ptrs_h = gdn.state_ptr_array([slots_h[1, 0].data_ptr(), d["state"][1].data_ptr()], "cuda")
+    ptrs_d = gdn.state_ptr_array([slots_d[1, 0].data_ptr(), d["state"][1].data_ptr()], "cuda")
+    gdn.gdn_forward_host(shape, h["q"], h["k"], h["v"], h["g"], h["beta"], ptrs_h, slots_h,
+                         out_h, 2, "gda")
+    with pytest.raises(gdn.GDNError) as e:
+        gdn.gdn_check_device_error()
+    assert e.value.status == gdn.GDN_ERR_DEVICE_ARG
+    gdn.gdn_forward(shape, d["q"], d["k"], d["v"], d["g"], d["beta"], ptrs_d, slots_d, out_d,
+                    2, "gda")
+    with pytest.raises(gdn.GDNError):
+        gdn.gdn_check_device_error()
+    gdn.gdn_check_device_error()  # cleared
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.cuda()[T:], out_d[T:])          # sequence 1 ran
+    assert torch.equal(slots_h[1].nan_to_num(7.0), slots_d[1].nan_to_num(7.0))
+    assert torch.isnan(out_h[:T]).all()                        # sequence 0 did not
